@@ -1,0 +1,216 @@
+/*
+ * pkvd.h -- paged-KV split-KV decode attention on GB300 (sm_103a): C ABI.
+ *
+ * One new query token per request is scored against that request's paged KV
+ * cache. The work is cut into splits along the sequence; each split runs an
+ * online softmax over its tokens and leaves a normalised P.V partial with its
+ * log-sum-exp, and a second kernel merges the splits of every (request,
+ * head). The operation is
+ *
+ *     out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[row(b,t,kv),:]) * V[row(b,t,kv),:Dv]
+ *     lse[b,h]   = ln sum_t exp(scale * q[b,h,:] . K[row(b,t,kv),:])
+ *
+ * with kv = h / (heads / kv_heads) and row(b,t,kv) = (page_table[b][t/ps] *
+ * kv_heads + kv) * ps + t % ps. Sources for the pieces:
+ *   - the split policy, the split-major grid and the head-dim-tiled merge:
+ *     aiter pull 4758, "[Gluon][MLA] Deeper async-copy pipeline in the bh16
+ *     stage-1 decode loop", Motivation and Technical Details 1-3;
+ *   - several keys per warp and xor-fold warp sums for the scores:
+ *     TensorFold pull 1932, "What this changes";
+ *   - the bank-conflict-free shared-memory pitch for K/V tiles:
+ *     ROCm/rocm-libraries pull 10102 (attention_dense LDS group padding),
+ *     Motivation and Technical Details.
+ *
+ * Two families:
+ *   GQA  head_dim D in {128, 256}, head_dim_v == D, heads / kv_heads in
+ *        {1, 2, 4, 8, 16}; K and V in separate pools.
+ *   MLA  head_dim 576 (512 no-rope + 64 rope), head_dim_v 512, kv_heads 1,
+ *        heads a multiple of 16; V is the first 512 elements of the same
+ *        576-wide row (pass v_pages == k_pages, both row pitches 576).
+ *
+ * Layouts (row-major, contiguous unless a pitch says otherwise):
+ *   q          [batch, heads, head_dim]                   bf16 or fp16
+ *   k_pages    [num_pool_pages, kv_heads, page_size, k_row_pitch]
+ *   v_pages    [num_pool_pages, kv_heads, page_size, v_row_pitch]
+ *   page_table [batch, max_pages_per_seq]                  int32 page ids
+ *   out        [batch, heads, head_dim_v]                  fp32
+ *   lse        [batch, heads]                              fp32, natural log
+ * Every device pointer must be 16-byte aligned, and each row pitch times the
+ * element size a multiple of 16 bytes.
+ *
+ * Ownership. The caller owns every tensor above. A plan owns its device work
+ * list and its partial workspace, allocated when the plan is made and freed
+ * by decode_plan_destroy. A plan holds a copy of seq_lens and is valid only
+ * for those lengths (and for the shapes it was made with): re-plan when they
+ * change.
+ *
+ * Errors. Every call returns a pkvd_status (0 = success) and never aborts.
+ * decode_run is asynchronous: it reports argument and launch errors only.
+ * Faults the kernels detect themselves (a page id outside the pool when
+ * checks are on, a pipeline wait that ran out) are recorded in a device
+ * status word and come back from decode_last_device_status.
+ *
+ * Streams. decode_run enqueues work on the given stream and neither
+ * allocates nor synchronises, so it can be captured in a CUDA graph.
+ */
+#ifndef PKVD_H_
+#define PKVD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pkvd_plan pkvd_plan;          /* opaque; immutable once made */
+typedef struct CUstream_st *pkvd_stream_t;   /* a cudaStream_t; NULL = legacy default stream */
+typedef struct CUevent_st *pkvd_event_t;     /* a cudaEvent_t */
+
+typedef enum pkvd_status {
+  PKVD_OK = 0,
+  PKVD_EINVAL = -1,         /* bad argument: null pointer, size, alignment  */
+  PKVD_EUNSUPPORTED = -2,   /* valid but unsupported shape or dtype         */
+  PKVD_ECUDA = -3,          /* a CUDA runtime call failed                   */
+  PKVD_ENOMEM = -4,         /* host or device allocation failed             */
+  PKVD_EDEVICE_CHECK = -5,  /* a kernel found a page id outside the pool    */
+  PKVD_ETIMEOUT = -6        /* a kernel's bounded pipeline wait ran out     */
+} pkvd_status;
+
+typedef enum pkvd_dtype { PKVD_BF16 = 0, PKVD_FP16 = 1 } pkvd_dtype;
+
+typedef enum pkvd_family { PKVD_FAMILY_GQA = 0, PKVD_FAMILY_MLA = 1 } pkvd_family;
+
+/* Stage-1 kernel variants. AUTO picks per shape. */
+typedef enum pkvd_variant {
+  PKVD_VARIANT_AUTO = 0,
+  PKVD_VARIANT_GQA_FMA = 1,   /* fp32 FMA scores and P.V, four keys per warp pass  */
+  PKVD_VARIANT_GQA_MMA = 2,   /* mma.sync m16n8k16: keys as M, the head group as N */
+  PKVD_VARIANT_MLA_MMA = 3    /* mma.sync, a block of 16 heads per work item       */
+} pkvd_variant;
+
+/* Order of stage-1 work items in the grid. Both orders compute the same
+ * items with the same reduction order, so results are bit-identical. */
+typedef enum pkvd_grid_order {
+  PKVD_ORDER_AUTO = 0,          /* split-major when batch > 1              */
+  PKVD_ORDER_SPLIT_MAJOR = 1,   /* item id = split-major over (s, b, unit) */
+  PKVD_ORDER_REQUEST_MAJOR = 2  /* item id = request-major over (b, unit, s) */
+} pkvd_grid_order;
+
+/* Full plan description. Zero in an optional field means "default". */
+typedef struct pkvd_plan_desc {
+  int32_t batch;              /* requests, >= 1                                   */
+  int32_t heads;              /* query heads per request                          */
+  int32_t kv_heads;           /* KV heads (MLA: 1)                                 */
+  int32_t head_dim;           /* D: 128, 256 (GQA) or 576 (MLA)                   */
+  int32_t head_dim_v;         /* Dv: 0 = D for GQA, 512 for MLA                   */
+  int32_t page_size;          /* tokens per page, >= 1                            */
+  int32_t dtype;              /* pkvd_dtype of q, K and V                         */
+  int32_t splits;             /* 0 = planner; > 0 = this many splits per request
+                                 (fewer when a request has fewer tokens)         */
+  int32_t grid_order;         /* pkvd_grid_order                                  */
+  int32_t stage2_tiles;       /* 0 = planner; else 1, 2, 4 or 8 slices of Dv      */
+  int32_t variant;            /* pkvd_variant                                     */
+  int32_t checks;             /* 1 = kernels bounds-check page ids (needs
+                                 num_pool_pages) and report via the status word  */
+  int32_t num_sms;            /* 0 = query the device                             */
+  int32_t ctas_per_sm;        /* 0 = query the occupancy of the chosen kernel     */
+  int32_t min_chunk;          /* 0 = default: smallest split, in tokens           */
+  int32_t reserved;           /* must be 0                                        */
+  int64_t max_pages_per_seq;  /* page_table row stride; 0 = max ceil(L_b / ps)    */
+  int64_t num_pool_pages;     /* pages in the pools; 0 = unknown (no checks)      */
+  int64_t k_row_pitch;        /* elements between K rows; 0 = D (MLA: 576)        */
+  int64_t v_row_pitch;        /* elements between V rows; 0 = Dv (MLA: 576)       */
+  float scale;                /* 0 = 1 / sqrt(D)                                  */
+  int32_t reserved2;          /* must be 0                                        */
+} pkvd_plan_desc;
+
+/* What the planner decided (decode_plan_query / decode_plan_compute). */
+typedef struct pkvd_plan_info {
+  int32_t family;             /* pkvd_family                                      */
+  int32_t variant;            /* resolved pkvd_variant                            */
+  int32_t grid_order;         /* resolved pkvd_grid_order                         */
+  int32_t stage2_tiles;       /* resolved slices of Dv in the merge               */
+  int32_t stage2_threads;     /* threads per merge block                          */
+  int32_t num_sms;            /* SMs the plan fills                               */
+  int32_t ctas_per_sm;        /* resident stage-1 blocks per SM                   */
+  int32_t heads_per_unit;     /* query heads one stage-1 item covers              */
+  int32_t units_per_request;  /* stage-1 items per (request, split)               */
+  int32_t num_items;          /* stage-1 grid size                                */
+  int32_t num_partial_rows;   /* sum over requests of their split counts          */
+  int32_t max_splits;         /* largest split count of any request               */
+  int64_t chunk;              /* tokens per split when uniform, else 0            */
+  int64_t workspace_bytes;    /* device bytes the plan owns                       */
+  int32_t block_tokens;       /* tokens per pipeline stage of the stage-1 kernel  */
+  int32_t pipeline_stages;    /* shared-memory stages of the stage-1 kernel       */
+  int32_t stage1_smem_bytes;  /* dynamic shared memory of a stage-1 block         */
+  int32_t stage1_threads;     /* threads of a stage-1 block                       */
+} pkvd_plan_info;
+
+/* One stage-1 work item as the planner lays it out (decode_plan_compute). */
+typedef struct pkvd_work_item {
+  int32_t request;            /* b                                                */
+  int32_t unit;               /* GQA: KV head; MLA: head block                    */
+  int32_t split;              /* s, 0-based within the request                    */
+  int32_t partial_row;        /* row of this split in the partial workspace      */
+  int32_t tok_begin;          /* first logical token                              */
+  int32_t tok_end;            /* one past the last logical token                 */
+  int32_t reserved0, reserved1;
+} pkvd_work_item;
+
+/* GQA shorthand of decode_plan_ex (head_dim_v = head_dim, bf16, all other
+ * fields default); head_dim 576 selects the MLA family (Dv 512, pitches 576).
+ * seq_lens: host array of `batch` lengths, copied. splits: 0 = planner. */
+int decode_plan(pkvd_plan **out, int batch, int heads, int kv_heads, int head_dim,
+                int page_size, const int32_t *seq_lens, int splits);
+
+/* Make a plan on the current CUDA device: checks the shape, runs the split
+ * planner, allocates and fills the device work list and the partial
+ * workspace. *out receives the plan (NULL on error). */
+int decode_plan_ex(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens);
+
+/* Launch stage 1 and the merge on `stream`. q, k_pages, v_pages, page_table,
+ * out and lse are device pointers laid out as above. Asynchronous. */
+int decode_run(const pkvd_plan *plan, const void *q, const void *k_pages,
+               const void *v_pages, const int32_t *page_table, float *out, float *lse,
+               pkvd_stream_t stream);
+
+/* decode_run that also records caller-made events on `stream`: ev_begin
+ * before stage 1, ev_mid between stage 1 and the merge, ev_end after the
+ * merge (any may be NULL). Recording ev_mid keeps the merge from overlapping
+ * stage 1's tail; otherwise identical to decode_run. For timing each stage. */
+int decode_run_timed(const pkvd_plan *plan, const void *q, const void *k_pages,
+                     const void *v_pages, const int32_t *page_table, float *out,
+                     float *lse, pkvd_stream_t stream, pkvd_event_t ev_begin,
+                     pkvd_event_t ev_mid, pkvd_event_t ev_end);
+
+/* Free a plan and its device memory (NULL is a no-op). Synchronises the
+ * plan's device so no run still reads the freed memory. */
+int decode_plan_destroy(pkvd_plan *plan);
+
+/* Device bytes the plan owns (work list, split table, partials, status). */
+size_t decode_workspace_bytes(const pkvd_plan *plan);
+
+/* Copy the planner's decisions into *info. */
+int decode_plan_query(const pkvd_plan *plan, pkvd_plan_info *info);
+
+/* Synchronise `stream`, then read and clear the plan's device status word:
+ * PKVD_OK, PKVD_EDEVICE_CHECK or PKVD_ETIMEOUT. */
+int decode_last_device_status(const pkvd_plan *plan, pkvd_stream_t stream);
+
+/* The split planner alone, on the host, with no CUDA call: desc->num_sms and
+ * desc->ctas_per_sm must be set (> 0). Fills *info and, when `items` is not
+ * NULL, up to `capacity` work items in grid order. Returns PKVD_OK, or
+ * PKVD_EINVAL when capacity is smaller than info->num_items (info is still
+ * filled). */
+int decode_plan_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
+                        pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
+
+/* Static description of a status code. */
+const char *decode_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKVD_H_ */

@@ -1,0 +1,197 @@
+"""Python surface of the C ABI: plan once, run many times.
+
+    plan = decode_plan(batch, heads, kv_heads, head_dim, page_size, seq_lens, splits)
+    decode_run(plan, q, k_pages, v_pages, page_table, out, lse)
+
+Tensors are torch CUDA tensors (PyTorch provides device memory and streams
+only). Shapes, dtypes and alignment are checked here; the arithmetic runs in
+the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import PlanDesc, PlanInfo, WorkItem, check
+
+_DTYPES = {torch.bfloat16: _lib.PKVD_BF16, torch.float16: _lib.PKVD_FP16,
+           "bf16": _lib.PKVD_BF16, "fp16": _lib.PKVD_FP16}
+
+
+def _seq_array(seq_lens) -> ctypes.Array:
+    vals = [int(x) for x in (seq_lens.tolist() if hasattr(seq_lens, "tolist") else seq_lens)]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def make_desc(batch: int, heads: int, kv_heads: int, head_dim: int, page_size: int, *,
+              head_dim_v: int = 0, dtype="bf16", splits: int = 0, grid_order: str = "auto",
+              stage2_tiles: int = 0, variant: str = "auto", checks: bool = False,
+              num_sms: int = 0, ctas_per_sm: int = 0, min_chunk: int = 0,
+              max_pages_per_seq: int = 0, num_pool_pages: int = 0, k_row_pitch: int = 0,
+              v_row_pitch: int = 0, scale: float = 0.0) -> PlanDesc:
+    d = PlanDesc()
+    d.batch, d.heads, d.kv_heads, d.head_dim = batch, heads, kv_heads, head_dim
+    d.head_dim_v, d.page_size, d.dtype = head_dim_v, page_size, _DTYPES[dtype]
+    d.splits, d.grid_order = splits, _lib.GRID_ORDERS[grid_order]
+    d.stage2_tiles, d.variant, d.checks = stage2_tiles, _lib.VARIANTS[variant], int(bool(checks))
+    d.num_sms, d.ctas_per_sm, d.min_chunk = num_sms, ctas_per_sm, min_chunk
+    d.max_pages_per_seq, d.num_pool_pages = max_pages_per_seq, num_pool_pages
+    d.k_row_pitch, d.v_row_pitch, d.scale = k_row_pitch, v_row_pitch, scale
+    return d
+
+
+class Plan:
+    """Owns a pkvd_plan* (freed on close / garbage collection)."""
+
+    def __init__(self, handle: ctypes.c_void_p, desc: PlanDesc):
+        self._h = handle
+        self.desc = desc
+        info = PlanInfo()
+        check(_lib.lib().decode_plan_query(self._h, ctypes.byref(info)), "decode_plan_query")
+        self.info = info.as_dict()
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise ValueError("plan was destroyed")
+        return self._h
+
+    def workspace_bytes(self) -> int:
+        return int(_lib.lib().decode_workspace_bytes(self.handle))
+
+    def last_device_status(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        return int(_lib.lib().decode_last_device_status(self.handle, ctypes.c_void_p(s)))
+
+    def close(self) -> None:
+        if self._h is not None:
+            check(_lib.lib().decode_plan_destroy(self._h), "decode_plan_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def decode_plan_ex(desc: PlanDesc, seq_lens: Sequence[int]) -> Plan:
+    h = ctypes.c_void_p()
+    check(_lib.lib().decode_plan_ex(ctypes.byref(h), ctypes.byref(desc),
+                                    ctypes.cast(_seq_array(seq_lens), ctypes.c_void_p)),
+          "decode_plan_ex")
+    return Plan(h, desc)
+
+
+def decode_plan(batch: int, heads: int, kv_heads: int, head_dim: int, page_size: int,
+                seq_lens: Sequence[int], splits: int = 0, **kw) -> Plan:
+    """Plan a decode op. Keyword arguments are the optional pkvd_plan_desc
+    fields (dtype, head_dim_v, grid_order, stage2_tiles, variant, checks, ...)."""
+    return decode_plan_ex(make_desc(batch, heads, kv_heads, head_dim, page_size,
+                                    splits=splits, **kw), seq_lens)
+
+
+def decode_plan_compute(desc: PlanDesc, seq_lens: Sequence[int], with_items: bool = True):
+    """The split planner alone, on the host (no CUDA): (info dict, work items)."""
+    L = _lib.lib()
+    info = PlanInfo()
+    seq = _seq_array(seq_lens)
+    check(L.decode_plan_compute(ctypes.byref(desc), ctypes.cast(seq, ctypes.c_void_p),
+                                ctypes.byref(info), None, 0), "decode_plan_compute")
+    items = []
+    if with_items and info.num_items > 0:
+        arr = (WorkItem * info.num_items)()
+        check(L.decode_plan_compute(ctypes.byref(desc), ctypes.cast(seq, ctypes.c_void_p),
+                                    ctypes.byref(info), ctypes.cast(arr, ctypes.c_void_p),
+                                    info.num_items), "decode_plan_compute")
+        items = [(w.request, w.unit, w.split, w.partial_row, w.tok_begin, w.tok_end)
+                 for w in arr]
+    return info.as_dict(), items
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensors(plan: Plan, q, k_pages, v_pages, page_table, out, lse) -> None:
+    d = plan.desc
+    dt = {_lib.PKVD_BF16: torch.bfloat16, _lib.PKVD_FP16: torch.float16}[d.dtype]
+    dv = d.head_dim_v or (512 if d.head_dim == 576 else d.head_dim)
+    for name, t, dtype in (("q", q, dt), ("k_pages", k_pages, dt), ("v_pages", v_pages, dt),
+                           ("page_table", page_table, torch.int32), ("out", out, torch.float32),
+                           ("lse", lse, torch.float32)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(q.shape) != (d.batch, d.heads, d.head_dim):
+        raise ValueError(f"q shape {tuple(q.shape)} != {(d.batch, d.heads, d.head_dim)}")
+    if tuple(out.shape) != (d.batch, d.heads, dv):
+        raise ValueError(f"out shape {tuple(out.shape)} != {(d.batch, d.heads, dv)}")
+    if tuple(lse.shape) != (d.batch, d.heads):
+        raise ValueError(f"lse shape {tuple(lse.shape)} != {(d.batch, d.heads)}")
+    if page_table.dim() != 2 or page_table.shape[0] != d.batch:
+        raise ValueError("page_table must be [batch, max_pages_per_seq]")
+
+
+def decode_run(plan: Plan, q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+               page_table: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+               stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Enqueue stage 1 and the merge on ``stream`` (default: current stream)."""
+    _check_tensors(plan, q, k_pages, v_pages, page_table, out, lse)
+    if plan.desc.max_pages_per_seq and page_table.shape[1] != plan.desc.max_pages_per_seq:
+        raise ValueError("page_table row length differs from the plan's max_pages_per_seq")
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    check(_lib.lib().decode_run(plan.handle, _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                _ptr(page_table), _ptr(out), _ptr(lse), ctypes.c_void_p(s)),
+          "decode_run")
+
+
+def decode_run_timed(plan: Plan, q, k_pages, v_pages, page_table, out, lse, ev_begin=None,
+                     ev_mid=None, ev_end=None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """decode_run that records torch.cuda.Events around and between the stages."""
+    _check_tensors(plan, q, k_pages, v_pages, page_table, out, lse)
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    for e in (ev_begin, ev_mid, ev_end):
+        if e is not None and not e.cuda_event:
+            e.record(stream or torch.cuda.current_stream())   # create the CUDA event
+    ev = [ctypes.c_void_p(e.cuda_event) if e is not None else None
+          for e in (ev_begin, ev_mid, ev_end)]
+    check(_lib.lib().decode_run_timed(plan.handle, _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                      _ptr(page_table), _ptr(out), _ptr(lse),
+                                      ctypes.c_void_p(s), *ev), "decode_run_timed")
+
+
+def plan_for_case(case, **kw) -> Plan:
+    """Plan matching a workloads.DecodeCase (splits from the case unless given)."""
+    kw.setdefault("splits", case.splits)
+    return decode_plan(case.batch, case.heads, case.kv_heads, case.head_dim, case.page_size,
+                       case.seq_lens.tolist(), head_dim_v=case.head_dim_v, dtype=case.dtype,
+                       max_pages_per_seq=case.max_pages, num_pool_pages=case.pool_pages,
+                       k_row_pitch=case.k_row_pitch, v_row_pitch=case.v_row_pitch,
+                       scale=case.scale, **kw)
+
+
+def run_case(plan: Plan, case_dev, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, stream=None):
+    """Run a plan on a DecodeCase whose tensors are on the GPU; returns (out, lse)."""
+    dev = case_dev.q.device
+    if out is None:
+        out = torch.empty((case_dev.batch, case_dev.heads, case_dev.head_dim_v),
+                          dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((case_dev.batch, case_dev.heads), dtype=torch.float32, device=dev)
+    decode_run(plan, case_dev.q, case_dev.k_pages, case_dev.v_pages, case_dev.page_table,
+               out, lse, stream)
+    return out, lse
+
+
+LN2 = math.log(2.0)

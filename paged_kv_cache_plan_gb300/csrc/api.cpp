@@ -1,0 +1,298 @@
+// The C ABI of include/pkvd.h: plan creation on the device, the two launches,
+// status handling. Argument marshalling only; all arithmetic is in the kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "../../include/pkvd.h"
+#include "kernel_configs.h"
+#include "kernels.h"
+#include "planner.h"
+
+struct pkvd_plan {
+  pkvd::PlanLayout layout;
+  int device = 0;
+  void* dmem = nullptr;
+  size_t dbytes = 0;
+  pkvd_work_item* d_items = nullptr;
+  int32_t* d_split_base = nullptr;
+  float* d_opart = nullptr;
+  float* d_lpart = nullptr;
+  int32_t* d_status = nullptr;
+  pkvd::KernelEntry s1;
+  pkvd::KernelEntry s2;
+  int s2_smem = 0;
+  float scale_log2 = 0.f;
+};
+
+namespace {
+
+constexpr double kLog2e = 1.4426950408889634074;
+
+bool kernel_for(int variant, int dtype, int head_dim, int group, pkvd::KernelEntry* e) {
+  switch (variant) {
+    case PKVD_VARIANT_GQA_FMA: return pkvd::gqa_fma_kernel(dtype, head_dim, group, e);
+    case PKVD_VARIANT_GQA_MMA: return pkvd::gqa_mma_kernel(dtype, head_dim, group, e);
+    case PKVD_VARIANT_MLA_MMA: return pkvd::mla_mma_kernel(dtype, e);
+    default: return false;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
+           const int32_t* page_table, float* out, float* lse, cudaStream_t stream,
+           cudaEvent_t ev_begin, cudaEvent_t ev_mid, cudaEvent_t ev_end) {
+  if (!p || !out || !lse) return PKVD_EINVAL;
+  const pkvd::PlanLayout& L = p->layout;
+  const pkvd_plan_desc& d = L.desc;
+  const bool any_work = L.info.num_items > 0;
+  if (any_work && (!q || !k || !v || !page_table)) return PKVD_EINVAL;
+  if (any_work && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(page_table)))
+    return PKVD_EINVAL;
+  if (!aligned16(out) || !aligned16(lse)) return PKVD_EINVAL;
+
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return PKVD_ECUDA;
+  if (cur != p->device) return PKVD_EINVAL;
+
+  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return PKVD_ECUDA;
+  if (any_work) {
+    pkvd::Stage1Args a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.page_table = page_table;
+    a.items = p->d_items;
+    a.o_part = p->d_opart;
+    a.lse_part = p->d_lpart;
+    a.status = p->d_status;
+    a.pt_stride = d.max_pages_per_seq;
+    a.k_pitch = d.k_row_pitch;
+    a.v_pitch = d.v_row_pitch;
+    a.num_pool_pages = d.num_pool_pages;
+    a.heads = d.heads;
+    a.kv_heads = d.kv_heads;
+    a.page_size = d.page_size;
+    a.dv = d.head_dim_v;
+    a.scale_log2 = p->scale_log2;
+    a.checks = d.checks;
+    void* args[] = {&a};
+    if (cudaLaunchKernel(p->s1.func, dim3(L.info.num_items), dim3(p->s1.threads), args,
+                         static_cast<size_t>(p->s1.smem), stream) != cudaSuccess)
+      return PKVD_ECUDA;
+  }
+  if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return PKVD_ECUDA;
+
+  pkvd::Stage2Args m{};
+  m.o_part = p->d_opart;
+  m.lse_part = p->d_lpart;
+  m.split_base = p->d_split_base;
+  m.out = out;
+  m.lse = lse;
+  m.heads = d.heads;
+  m.dv = d.head_dim_v;
+  m.tiles = L.info.stage2_tiles;
+  void* margs[] = {&m};
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(d.batch * d.heads), static_cast<unsigned>(m.tiles));
+  cfg.blockDim = dim3(static_cast<unsigned>(L.info.stage2_threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(p->s2_smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = any_work ? 1 : 0;
+  if (cudaLaunchKernelExC(&cfg, p->s2.func, margs) != cudaSuccess) return PKVD_ECUDA;
+  if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return PKVD_ECUDA;
+  return PKVD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_plan_compute(const pkvd_plan_desc* desc, const int32_t* seq_lens,
+                        pkvd_plan_info* info, pkvd_work_item* items, int64_t capacity) {
+  if (!desc || !info) return PKVD_EINVAL;
+  pkvd::PlanLayout L;
+  int rc;
+  try {
+    rc = pkvd::plan_layout(*desc, seq_lens, &L);
+  } catch (const std::bad_alloc&) {
+    return PKVD_ENOMEM;
+  }
+  if (rc != PKVD_OK) return rc;
+  *info = L.info;
+  if (items) {
+    if (capacity < L.info.num_items) return PKVD_EINVAL;
+    std::memcpy(items, L.items.data(), L.items.size() * sizeof(pkvd_work_item));
+  }
+  return PKVD_OK;
+}
+
+int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens) {
+  if (!out || !desc) return PKVD_EINVAL;
+  *out = nullptr;
+  pkvd_plan_desc d;
+  int family = 0;
+  int rc = pkvd::normalise_desc(*desc, seq_lens, &d, &family);
+  if (rc != PKVD_OK) return rc;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
+  pkvd::KernelEntry s1, s2;
+  const int group = d.heads / d.kv_heads;
+  if (!kernel_for(d.variant, d.dtype, d.head_dim, group, &s1)) return PKVD_EUNSUPPORTED;
+  pkvd::stage2_kernel(&s2);
+  if (d.num_sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKVD_ECUDA;
+    d.num_sms = sms;
+  }
+  if (cudaFuncSetAttribute(s1.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1.smem) !=
+      cudaSuccess)
+    return PKVD_ECUDA;
+  if (d.ctas_per_sm == 0) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, s1.func, s1.threads,
+                                                      static_cast<size_t>(s1.smem)) !=
+        cudaSuccess)
+      return PKVD_ECUDA;
+    if (occ < 1) return PKVD_EUNSUPPORTED;
+    d.ctas_per_sm = occ;
+  }
+
+  pkvd_plan* p = new (std::nothrow) pkvd_plan;
+  if (!p) return PKVD_ENOMEM;
+  try {
+    rc = pkvd::plan_layout(d, seq_lens, &p->layout);
+  } catch (const std::bad_alloc&) {
+    rc = PKVD_ENOMEM;
+  }
+  if (rc != PKVD_OK) {
+    delete p;
+    return rc;
+  }
+  p->device = dev;
+  p->s1 = s1;
+  p->s2 = s2;
+  const pkvd::PlanLayout& L = p->layout;
+  p->s2_smem = std::max(1, L.info.max_splits) * 4;
+  p->scale_log2 = static_cast<float>(static_cast<double>(L.desc.scale) * kLog2e);
+
+  // one device allocation, carved in 256-byte aligned pieces
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = static_cast<size_t>(std::max(1, L.info.num_partial_rows));
+  const size_t b_items = al(std::max<size_t>(L.items.size(), 1) * sizeof(pkvd_work_item));
+  const size_t b_split = al(static_cast<size_t>(L.desc.batch + 1) * 4);
+  const size_t b_opart = al(rows * L.desc.heads * L.desc.head_dim_v * 4);
+  const size_t b_lpart = al(rows * L.desc.heads * 4);
+  const size_t b_status = al(16);
+  p->dbytes = b_items + b_split + b_opart + b_lpart + b_status;
+  if (cudaMalloc(&p->dmem, p->dbytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return PKVD_ENOMEM;
+  }
+  char* base = static_cast<char*>(p->dmem);
+  p->d_items = reinterpret_cast<pkvd_work_item*>(base);
+  p->d_split_base = reinterpret_cast<int32_t*>(base + b_items);
+  p->d_opart = reinterpret_cast<float*>(base + b_items + b_split);
+  p->d_lpart = reinterpret_cast<float*>(base + b_items + b_split + b_opart);
+  p->d_status = reinterpret_cast<int32_t*>(base + b_items + b_split + b_opart + b_lpart);
+  bool ok = true;
+  if (!L.items.empty())
+    ok = ok && cudaMemcpy(p->d_items, L.items.data(), L.items.size() * sizeof(pkvd_work_item),
+                          cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemcpy(p->d_split_base, L.split_base.data(), (L.desc.batch + 1) * 4,
+                        cudaMemcpyHostToDevice) == cudaSuccess;
+  ok = ok && cudaMemset(p->d_status, 0, 16) == cudaSuccess;
+  if (!ok) {
+    cudaFree(p->dmem);
+    delete p;
+    return PKVD_ECUDA;
+  }
+  *out = p;
+  return PKVD_OK;
+}
+
+int decode_plan(pkvd_plan** out, int batch, int heads, int kv_heads, int head_dim, int page_size,
+                const int32_t* seq_lens, int splits) {
+  pkvd_plan_desc d{};
+  d.batch = batch;
+  d.heads = heads;
+  d.kv_heads = kv_heads;
+  d.head_dim = head_dim;
+  d.page_size = page_size;
+  d.splits = splits;
+  d.dtype = PKVD_BF16;
+  return decode_plan_ex(out, &d, seq_lens);
+}
+
+int decode_run(const pkvd_plan* plan, const void* q, const void* k_pages, const void* v_pages,
+               const int32_t* page_table, float* out, float* lse, pkvd_stream_t stream) {
+  return launch(plan, q, k_pages, v_pages, page_table, out, lse,
+                reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr);
+}
+
+int decode_run_timed(const pkvd_plan* plan, const void* q, const void* k_pages,
+                     const void* v_pages, const int32_t* page_table, float* out, float* lse,
+                     pkvd_stream_t stream, pkvd_event_t ev_begin, pkvd_event_t ev_mid,
+                     pkvd_event_t ev_end) {
+  return launch(plan, q, k_pages, v_pages, page_table, out, lse,
+                reinterpret_cast<cudaStream_t>(stream), reinterpret_cast<cudaEvent_t>(ev_begin),
+                reinterpret_cast<cudaEvent_t>(ev_mid), reinterpret_cast<cudaEvent_t>(ev_end));
+}
+
+int decode_plan_destroy(pkvd_plan* plan) {
+  if (!plan) return PKVD_OK;
+  int rc = PKVD_OK;
+  int cur = 0;
+  if (cudaGetDevice(&cur) == cudaSuccess && cur != plan->device) cudaSetDevice(plan->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) rc = PKVD_ECUDA;
+  if (plan->dmem && cudaFree(plan->dmem) != cudaSuccess) rc = PKVD_ECUDA;
+  if (cur != plan->device) cudaSetDevice(cur);
+  delete plan;
+  return rc;
+}
+
+size_t decode_workspace_bytes(const pkvd_plan* plan) { return plan ? plan->dbytes : 0; }
+
+int decode_plan_query(const pkvd_plan* plan, pkvd_plan_info* info) {
+  if (!plan || !info) return PKVD_EINVAL;
+  *info = plan->layout.info;
+  info->workspace_bytes = static_cast<int64_t>(plan->dbytes);
+  return PKVD_OK;
+}
+
+int decode_last_device_status(const pkvd_plan* plan, pkvd_stream_t stream) {
+  if (!plan) return PKVD_EINVAL;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKVD_ECUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, plan->d_status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return PKVD_ECUDA;
+  if (v != 0 && cudaMemset(plan->d_status, 0, 4) != cudaSuccess) return PKVD_ECUDA;
+  if (v & 1) return PKVD_ETIMEOUT;
+  if (v & 2) return PKVD_EDEVICE_CHECK;
+  return PKVD_OK;
+}
+
+const char* decode_status_string(int status) {
+  switch (status) {
+    case PKVD_OK: return "ok";
+    case PKVD_EINVAL: return "invalid argument";
+    case PKVD_EUNSUPPORTED: return "unsupported shape or dtype";
+    case PKVD_ECUDA: return "CUDA runtime error";
+    case PKVD_ENOMEM: return "out of memory";
+    case PKVD_EDEVICE_CHECK: return "a kernel found a page id outside the pool";
+    case PKVD_ETIMEOUT: return "a kernel pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

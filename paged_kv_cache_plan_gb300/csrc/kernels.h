@@ -1,0 +1,59 @@
+// Kernel arguments and the per-variant kernel lookup shared by the host
+// launcher and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/pkvd.h"
+
+namespace pkvd {
+
+// Arguments of every stage-1 kernel (one work item per block).
+struct Stage1Args {
+  const void* q;                 // [B, Hq, D] 16-bit
+  const void* k;                 // K pool, rows of k_pitch elements
+  const void* v;                 // V pool, rows of v_pitch elements
+  const int32_t* page_table;     // [B, pt_stride]
+  const pkvd_work_item* items;   // [grid]
+  float* o_part;                 // [rows, Hq, Dv] normalised partial outputs
+  float* lse_part;               // [rows, Hq] partial log2-sum-exp2 (log2 domain)
+  int32_t* status;               // device status word (kStatus* bits)
+  int64_t pt_stride;             // entries per page_table row
+  int64_t k_pitch;               // elements between K rows
+  int64_t v_pitch;               // elements between V rows
+  int64_t num_pool_pages;        // pages in the pools (checks only)
+  int32_t heads;                 // Hq
+  int32_t kv_heads;              // Hkv
+  int32_t page_size;             // tokens per page
+  int32_t dv;                    // Dv
+  float scale_log2;              // scale * log2(e): scores go straight to exp2
+  int32_t checks;                // 1 = bounds-check page ids
+};
+
+// Arguments of the merge kernel (one block per (request, head, Dv slice)).
+struct Stage2Args {
+  const float* o_part;
+  const float* lse_part;
+  const int32_t* split_base;     // [B + 1] first partial row of each request
+  float* out;                    // [B, Hq, Dv]
+  float* lse;                    // [B, Hq] natural log
+  int32_t heads;
+  int32_t dv;
+  int32_t tiles;                 // Dv slices (gridDim.y)
+};
+
+struct KernelEntry {
+  const void* func = nullptr;    // __global__ symbol, launched with one Stage*Args
+  int threads = 0;
+  int smem = 0;                  // dynamic shared memory bytes
+  int block_tokens = 0;
+  int stages = 0;
+};
+
+// Lookups; false when the combination has no kernel.
+bool gqa_fma_kernel(int dtype, int head_dim, int group, KernelEntry* e);
+bool gqa_mma_kernel(int dtype, int head_dim, int group, KernelEntry* e);
+bool mla_mma_kernel(int dtype, KernelEntry* e);
+bool stage2_kernel(KernelEntry* e);
+
+}  // namespace pkvd

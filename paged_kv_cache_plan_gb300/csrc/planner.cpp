@@ -1,0 +1,265 @@
+// Split planner (host). See planner.h.
+//
+// Split policy. The aiter pull 4758 page (Motivation) gives each request
+// about 256/batch splits on a 256-CU part, trading split count against how
+// far each stage-1 program walks. Here the same trade is made against this
+// GPU's stage-1 capacity: a uniform chunk of C tokens (a multiple of the
+// kernel's block) is the smallest one for which the work items
+//     sum_b units * ceil(L_b / C)
+// fit in one wave of num_sms * ctas_per_sm resident blocks; request b then
+// has S_b = ceil(L_b / C) splits. A forced split count S gives request b the
+// chunk ceil(L_b / S) instead (so min(S, L_b) splits).
+//
+// Grid order (the same page, Technical Details 2): split-major puts all
+// requests' items of one split next to each other (L2 reuse under prefix
+// sharing); it is a pure relabelling, so results are bit-identical.
+//
+// Merge tiling (the same page, Technical Details 3): slice Dv only while
+// the B * Hq merge blocks would leave SMs idle, up to 8 ways, and only into
+// slices that divide Dv evenly.
+#include "planner.h"
+
+#include <algorithm>
+#include <cmath>
+
+#include "kernel_configs.h"
+
+namespace pkvd {
+
+namespace {
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+bool variant_shape(int variant, int head_dim, int group, VariantShape* out) {
+  switch (variant) {
+    case PKVD_VARIANT_GQA_FMA:
+      if ((head_dim != 128 && head_dim != 256) || !is_pow2(group) || group > 8) return false;
+      *out = {kGqaBlockTokens, gqa_stages(head_dim), kStage1Threads,
+              gqa_smem_bytes(head_dim, group)};
+      return true;
+    case PKVD_VARIANT_GQA_MMA:
+      if ((head_dim != 128 && head_dim != 256) || group < 1 || group > 16) return false;
+      *out = {kGqaBlockTokens, gqa_stages(head_dim), kStage1Threads,
+              gqa_smem_bytes(head_dim, group > 8 ? 16 : 8)};
+      return true;
+    case PKVD_VARIANT_MLA_MMA:
+      if (head_dim != kMlaDk) return false;
+      *out = {kMlaBlockTokens, kMlaStages, kStage1Threads, kMlaSmemBytes};
+      return true;
+    default:
+      return false;
+  }
+}
+
+int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_desc* out,
+                   int* family) {
+  pkvd_plan_desc d = in;
+  if (!seq_lens && d.batch > 0) return PKVD_EINVAL;
+  if (d.batch < 1 || d.heads < 1 || d.kv_heads < 1 || d.head_dim < 1 || d.page_size < 1)
+    return PKVD_EINVAL;
+  if (d.head_dim_v < 0 || d.splits < 0 || d.num_sms < 0 || d.ctas_per_sm < 0 ||
+      d.min_chunk < 0 || d.max_pages_per_seq < 0 || d.num_pool_pages < 0 ||
+      d.k_row_pitch < 0 || d.v_row_pitch < 0)
+    return PKVD_EINVAL;
+  if (d.reserved != 0 || d.reserved2 != 0) return PKVD_EINVAL;
+  if (d.dtype != PKVD_BF16 && d.dtype != PKVD_FP16) return PKVD_EINVAL;
+  if (d.grid_order < PKVD_ORDER_AUTO || d.grid_order > PKVD_ORDER_REQUEST_MAJOR)
+    return PKVD_EINVAL;
+  if (d.stage2_tiles != 0 && d.stage2_tiles != 1 && d.stage2_tiles != 2 &&
+      d.stage2_tiles != 4 && d.stage2_tiles != 8)
+    return PKVD_EINVAL;
+  if (d.checks != 0 && d.checks != 1) return PKVD_EINVAL;
+  if (d.checks && d.num_pool_pages == 0) return PKVD_EINVAL;
+  if (!(std::isfinite(d.scale)) || d.scale < 0.f) return PKVD_EINVAL;
+  if (d.heads % d.kv_heads != 0) return PKVD_EUNSUPPORTED;
+
+  const bool mla = d.head_dim == kMlaDk;
+  if (mla) {
+    if (d.head_dim_v == 0) d.head_dim_v = kMlaDv;
+    if (d.head_dim_v != kMlaDv || d.kv_heads != 1 || d.heads % kMlaHeads != 0)
+      return PKVD_EUNSUPPORTED;
+    if (d.k_row_pitch == 0) d.k_row_pitch = kMlaDk;
+    if (d.v_row_pitch == 0) d.v_row_pitch = kMlaDk;
+    if (d.k_row_pitch != d.v_row_pitch) return PKVD_EUNSUPPORTED;   // V aliases K rows
+  } else {
+    if (d.head_dim != 128 && d.head_dim != 256) return PKVD_EUNSUPPORTED;
+    if (d.head_dim_v == 0) d.head_dim_v = d.head_dim;
+    if (d.head_dim_v != d.head_dim) return PKVD_EUNSUPPORTED;
+    if (d.k_row_pitch == 0) d.k_row_pitch = d.head_dim;
+    if (d.v_row_pitch == 0) d.v_row_pitch = d.head_dim_v;
+  }
+  if (d.k_row_pitch < d.head_dim || d.v_row_pitch < d.head_dim_v) return PKVD_EINVAL;
+  if ((d.k_row_pitch * 2) % 16 != 0 || (d.v_row_pitch * 2) % 16 != 0) return PKVD_EINVAL;
+  if (d.scale == 0.f) d.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+
+  int64_t max_pages = 0;
+  for (int b = 0; b < d.batch; ++b) {
+    if (seq_lens[b] < 0) return PKVD_EINVAL;
+    max_pages = std::max<int64_t>(max_pages, ceil_div(seq_lens[b], d.page_size));
+  }
+  if (d.max_pages_per_seq == 0) d.max_pages_per_seq = std::max<int64_t>(1, max_pages);
+  if (d.max_pages_per_seq < max_pages) return PKVD_EINVAL;
+
+  const int group = d.heads / d.kv_heads;
+  if (mla) {
+    if (d.variant == PKVD_VARIANT_AUTO) d.variant = PKVD_VARIANT_MLA_MMA;
+    if (d.variant != PKVD_VARIANT_MLA_MMA) return PKVD_EUNSUPPORTED;
+  } else {
+    if (d.variant == PKVD_VARIANT_AUTO)
+      d.variant = (is_pow2(group) && group <= 8) ? PKVD_VARIANT_GQA_FMA : PKVD_VARIANT_GQA_MMA;
+    if (d.variant != PKVD_VARIANT_GQA_FMA && d.variant != PKVD_VARIANT_GQA_MMA)
+      return PKVD_EUNSUPPORTED;
+  }
+  VariantShape vs;
+  if (!variant_shape(d.variant, d.head_dim, group, &vs)) return PKVD_EUNSUPPORTED;
+  *out = d;
+  *family = mla ? PKVD_FAMILY_MLA : PKVD_FAMILY_GQA;
+  return PKVD_OK;
+}
+
+int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* out) {
+  pkvd_plan_desc d;
+  int family = 0;
+  int rc = normalise_desc(in, seq_lens, &d, &family);
+  if (rc != PKVD_OK) return rc;
+  if (d.num_sms < 1 || d.ctas_per_sm < 1) return PKVD_EINVAL;
+
+  const int B = d.batch;
+  const int group = d.heads / d.kv_heads;
+  VariantShape vs;
+  variant_shape(d.variant, d.head_dim, group, &vs);
+  const int blk = vs.block_tokens;
+
+  PlanLayout& P = *out;
+  P.desc = d;
+  P.seq_lens.assign(seq_lens, seq_lens + B);
+  P.splits.assign(B, 0);
+  P.split_base.assign(B + 1, 0);
+  P.items.clear();
+
+  pkvd_plan_info& I = P.info;
+  I = pkvd_plan_info{};
+  I.family = family;
+  I.variant = d.variant;
+  I.num_sms = d.num_sms;
+  I.ctas_per_sm = d.ctas_per_sm;
+  if (family == PKVD_FAMILY_MLA) {
+    I.heads_per_unit = kMlaHeads;
+    I.units_per_request = d.heads / kMlaHeads;
+  } else {
+    I.heads_per_unit = group;
+    I.units_per_request = d.kv_heads;
+  }
+  I.block_tokens = blk;
+  I.pipeline_stages = vs.stages;
+  I.stage1_smem_bytes = vs.smem;
+  I.stage1_threads = vs.threads;
+  const int units = I.units_per_request;
+
+  // --- split sizes
+  std::vector<int64_t> chunk(B, 1);
+  int64_t maxL = 0;
+  for (int b = 0; b < B; ++b) maxL = std::max<int64_t>(maxL, P.seq_lens[b]);
+  if (d.splits > 0) {
+    for (int b = 0; b < B; ++b) {
+      const int64_t L = P.seq_lens[b];
+      chunk[b] = std::max<int64_t>(1, ceil_div(L, d.splits));
+      P.splits[b] = L == 0 ? 0 : static_cast<int32_t>(ceil_div(L, chunk[b]));
+    }
+    bool uniform = true;
+    for (int b = 1; b < B; ++b) uniform = uniform && chunk[b] == chunk[0];
+    I.chunk = uniform ? chunk[0] : 0;
+  } else {
+    const int64_t target = static_cast<int64_t>(d.num_sms) * d.ctas_per_sm;
+    const int64_t min_chunk =
+        std::max<int64_t>(blk, ceil_div(d.min_chunk > 0 ? d.min_chunk : 2 * blk, blk) * blk);
+    auto items_for = [&](int64_t C) {
+      int64_t n = 0;
+      for (int b = 0; b < B; ++b) n += ceil_div(P.seq_lens[b], C);
+      return n * units;
+    };
+    // smallest multiple of blk (>= min_chunk) whose items fit one wave,
+    // else one split per request
+    const int64_t hi_c = std::max<int64_t>(min_chunk, ceil_div(std::max<int64_t>(maxL, 1), blk) * blk);
+    int64_t C = hi_c;
+    if (items_for(hi_c) <= target) {
+      int64_t lo = ceil_div(min_chunk, blk), hi = hi_c / blk;   // in blocks
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        if (items_for(mid * blk) <= target) hi = mid; else lo = mid + 1;
+      }
+      C = lo * blk;
+    }
+    // the merge keeps one weight per split in shared memory
+    while (ceil_div(maxL, C) > kMaxSplits) C += blk;
+    for (int b = 0; b < B; ++b) {
+      chunk[b] = C;
+      P.splits[b] = static_cast<int32_t>(ceil_div(P.seq_lens[b], C));
+    }
+    I.chunk = C;
+  }
+  int max_s = 0;
+  for (int b = 0; b < B; ++b) {
+    if (P.splits[b] > kMaxSplits) return PKVD_EUNSUPPORTED;
+    P.split_base[b + 1] = P.split_base[b] + P.splits[b];
+    max_s = std::max(max_s, P.splits[b]);
+  }
+  I.num_partial_rows = P.split_base[B];
+  I.max_splits = max_s;
+
+  // --- work list
+  int order = d.grid_order;
+  if (order == PKVD_ORDER_AUTO) order = B > 1 ? PKVD_ORDER_SPLIT_MAJOR : PKVD_ORDER_REQUEST_MAJOR;
+  I.grid_order = order;
+  auto push = [&](int b, int u, int s) {
+    pkvd_work_item w{};
+    w.request = b;
+    w.unit = u;
+    w.split = s;
+    w.partial_row = P.split_base[b] + s;
+    w.tok_begin = static_cast<int32_t>(s * chunk[b]);
+    w.tok_end = static_cast<int32_t>(std::min<int64_t>(P.seq_lens[b], (s + 1) * chunk[b]));
+    P.items.push_back(w);
+  };
+  if (order == PKVD_ORDER_SPLIT_MAJOR) {
+    for (int s = 0; s < max_s; ++s)
+      for (int b = 0; b < B; ++b)
+        if (s < P.splits[b])
+          for (int u = 0; u < units; ++u) push(b, u, s);
+  } else {
+    for (int b = 0; b < B; ++b)
+      for (int u = 0; u < units; ++u)
+        for (int s = 0; s < P.splits[b]; ++s) push(b, u, s);
+  }
+  I.num_items = static_cast<int32_t>(P.items.size());
+
+  // --- merge tiling
+  const int dv = d.head_dim_v;
+  int tiles = d.stage2_tiles;
+  const int64_t base = static_cast<int64_t>(B) * d.heads;
+  if (tiles == 0) {
+    tiles = 1;
+    while (tiles < 8 && base * tiles * 2 <= d.num_sms && dv % (tiles * 2 * 32) == 0) tiles *= 2;
+  } else if (dv % (tiles * 4) != 0) {
+    return PKVD_EUNSUPPORTED;
+  }
+  I.stage2_tiles = tiles;
+  const int per_tile = dv / tiles;
+  I.stage2_threads = std::min(256, std::max(32, ((per_tile / 4 + 31) / 32) * 32));
+
+  // --- workspace: items, split table, partial outputs and lse, status word
+  auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t rows = I.num_partial_rows;
+  I.workspace_bytes = al(static_cast<int64_t>(std::max<size_t>(P.items.size(), 1)) *
+                         static_cast<int64_t>(sizeof(pkvd_work_item))) +
+                      al(static_cast<int64_t>(B + 1) * 4) +
+                      al(std::max<int64_t>(rows, 1) * d.heads * dv * 4) +
+                      al(std::max<int64_t>(rows, 1) * d.heads * 4) + al(16);
+  return PKVD_OK;
+}
+
+}  // namespace pkvd

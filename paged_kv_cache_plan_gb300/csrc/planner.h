@@ -1,0 +1,38 @@
+// Host split planner: shape checks, variant choice, split sizes, work-list
+// order and merge tiling. Plain C++; no CUDA call anywhere in it.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/pkvd.h"
+
+namespace pkvd {
+
+struct PlanLayout {
+  pkvd_plan_desc desc{};             // normalised (defaults filled in)
+  pkvd_plan_info info{};
+  std::vector<int32_t> seq_lens;
+  std::vector<int32_t> splits;       // S_b
+  std::vector<int32_t> split_base;   // B + 1 prefix sums of S_b
+  std::vector<pkvd_work_item> items; // stage-1 grid order
+};
+
+// Static per-variant numbers the planner needs (block tokens, stages,
+// threads, shared memory); false when the variant has no kernel for the shape.
+struct VariantShape {
+  int block_tokens;
+  int stages;
+  int threads;
+  int smem;
+};
+bool variant_shape(int variant, int head_dim, int group, VariantShape* out);
+
+// Validate and normalise `in`; resolve the family and (if AUTO) the variant.
+int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_desc* out,
+                   int* family);
+
+// Full planning with desc->num_sms and desc->ctas_per_sm already set (> 0).
+int plan_layout(const pkvd_plan_desc& desc, const int32_t* seq_lens, PlanLayout* out);
+
+}  // namespace pkvd

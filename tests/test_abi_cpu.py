@@ -1,0 +1,174 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared entry
+point, and its host planner (decode_plan_compute, no CUDA call) lays out the
+splits, grid order and merge tiling as documented. No kernel runs here."""
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_plan_gb300 import _lib, decode_plan_compute, make_desc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_cache_plan_gb300 import build
+    build.build()
+    return _lib.lib()
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "pkvd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*(\w+)\s*\(", src, re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), f"libpkvd.so does not export {n}"
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert _lib.status_string(code) not in ("", "unknown status")
+    assert _lib.status_string(123) == "unknown status"
+
+
+def _plan(*args, seq, **kw):
+    kw.setdefault("num_sms", 152)
+    kw.setdefault("ctas_per_sm", 1)
+    return decode_plan_compute(make_desc(*args, **kw), seq)
+
+
+def _check_cover(info, items, seq, units):
+    # every (request, unit) token range is covered exactly once, in split order
+    by = {}
+    for (b, u, s, row, t0, t1) in items:
+        by.setdefault((b, u), []).append((s, t0, t1, row))
+    for b, L in enumerate(seq):
+        for u in range(units):
+            got = sorted(by.get((b, u), []))
+            if L == 0:
+                assert not got
+                continue
+            assert [g[0] for g in got] == list(range(len(got)))
+            assert got[0][1] == 0 and got[-1][2] == L
+            for a, c in zip(got, got[1:]):
+                assert a[2] == c[1] and a[1] < a[2]
+    rows = sorted({(b, s, row) for (b, u, s, row, t0, t1) in items})
+    assert len({r for (_, _, r) in rows}) == info["num_partial_rows"]
+
+
+def test_auto_split_fills_one_wave(L):
+    for seq, sms, occ in (([65536], 152, 1), ([65536], 152, 2), ([2048], 152, 2),
+                          ([256, 512, 768, 1024, 1536, 2048, 8192, 32768, 65536, 131072], 152, 2)):
+        kv = 2 if len(seq) == 1 else 8
+        heads = 16 if kv == 2 else 32
+        d = 256 if kv == 2 else 128
+        info, items = _plan(len(seq), heads, kv, d, 16, seq=seq, num_sms=sms, ctas_per_sm=occ)
+        assert info["num_items"] <= sms * occ
+        assert info["chunk"] % 16 == 0
+        _check_cover(info, items, seq, kv)
+        # a smaller chunk would need more than one wave
+        C = info["chunk"] - 16
+        if C >= 32:
+            assert sum(-(-L // C) for L in seq) * kv > sms * occ
+
+
+def test_forced_splits(L):
+    info, items = _plan(1, 4, 1, 128, 16, seq=[512], splits=4)
+    assert info["num_items"] == 4 and info["chunk"] == 128
+    assert [(t0, t1) for (*_, t0, t1) in items] == [(0, 128), (128, 256), (256, 384), (384, 512)]
+    # more splits than tokens: one token each
+    info, items = _plan(1, 4, 1, 128, 16, seq=[10], splits=64)
+    assert info["num_items"] == 10 and info["max_splits"] == 10
+    # MLA policy 256 / batch at 68,000 tokens
+    for B in (1, 8, 24, 48):
+        info, items = _plan(B, 16, 1, 576, 1, seq=[68000] * B, splits=max(1, 256 // B))
+        assert info["max_splits"] == 256 // B
+        _check_cover(info, items, [68000] * B, 1)
+
+
+def test_grid_orders_same_items(L):
+    seq = [100, 0, 37, 300]
+    a_info, a = _plan(4, 8, 2, 128, 16, seq=seq, grid_order="split_major", splits=3)
+    b_info, b = _plan(4, 8, 2, 128, 16, seq=seq, grid_order="request_major", splits=3)
+    assert a_info["grid_order"] == 1 and b_info["grid_order"] == 2
+    assert sorted(a) == sorted(b) and a != b
+    # split-major: split index never decreases along the grid
+    assert [it[2] for it in a] == sorted(it[2] for it in a)
+    auto1, _ = _plan(1, 8, 2, 128, 16, seq=[100])
+    auto4, _ = _plan(4, 8, 2, 128, 16, seq=seq)
+    assert auto1["grid_order"] == 2 and auto4["grid_order"] == 1
+
+
+def test_stage2_tiling_gate(L):
+    # batch 1, 16 heads on 152 SMs: idle machine -> 8 slices of 512
+    info, _ = _plan(1, 16, 1, 576, 1, seq=[68000])
+    assert info["stage2_tiles"] == 8
+    # many heads: the grid already fills the machine -> untiled
+    info, _ = _plan(64, 128, 1, 576, 1, seq=[16384] * 64)
+    assert info["stage2_tiles"] == 1
+    # d 128 cannot be cut into 8 slices of at least 32
+    info, _ = _plan(1, 4, 1, 128, 16, seq=[512])
+    assert info["stage2_tiles"] == 4
+    info, _ = _plan(1, 4, 1, 128, 16, seq=[512], stage2_tiles=2)
+    assert info["stage2_tiles"] == 2
+
+
+def test_variant_resolution(L):
+    assert _plan(1, 16, 2, 256, 16, seq=[10])[0]["variant"] == 1      # FMA, group 8
+    assert _plan(1, 32, 2, 128, 16, seq=[10])[0]["variant"] == 2      # MMA, group 16
+    assert _plan(1, 16, 2, 256, 16, seq=[10], variant="gqa_mma")[0]["variant"] == 2
+    assert _plan(1, 128, 1, 576, 1, seq=[10])[0]["variant"] == 3
+    info = _plan(2, 128, 1, 576, 1, seq=[10, 20])[0]
+    assert info["units_per_request"] == 8 and info["heads_per_unit"] == 16
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(args=(1, 6, 4, 128, 16)), _lib.PKVD_EUNSUPPORTED),        # heads % kv_heads
+    (dict(args=(1, 4, 1, 96, 16)), _lib.PKVD_EUNSUPPORTED),         # head_dim
+    (dict(args=(1, 8, 2, 576, 1)), _lib.PKVD_EUNSUPPORTED),         # MLA with kv_heads 2
+    (dict(args=(1, 24, 1, 576, 1)), _lib.PKVD_EUNSUPPORTED),        # MLA heads % 16
+    (dict(args=(1, 4, 1, 128, 0)), _lib.PKVD_EINVAL),               # page size
+    (dict(args=(0, 4, 1, 128, 16)), _lib.PKVD_EINVAL),              # batch
+    (dict(args=(1, 4, 1, 128, 16), checks=True), _lib.PKVD_EINVAL), # checks need the pool size
+    (dict(args=(1, 4, 1, 128, 16), stage2_tiles=3), _lib.PKVD_EINVAL),
+    (dict(args=(1, 4, 1, 128, 16), k_row_pitch=100), _lib.PKVD_EINVAL),   # pitch < D
+    (dict(args=(1, 4, 1, 128, 16), k_row_pitch=132), _lib.PKVD_EINVAL),   # 264 B not 16-B aligned
+    (dict(args=(1, 4, 1, 128, 16), max_pages_per_seq=3), _lib.PKVD_EINVAL),
+    (dict(args=(1, 32, 1, 128, 16), variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),
+    (dict(args=(1, 4, 1, 128, 16), variant="mla_mma"), _lib.PKVD_EUNSUPPORTED),
+])
+def test_argument_errors(L, kw, code):
+    args = kw.pop("args")
+    with pytest.raises(_lib.PkvdError) as e:
+        _plan(*args, seq=[100] * args[0] if args[0] > 0 else [], **kw)
+    assert e.value.code == code
+
+
+def test_negative_length_rejected(L):
+    with pytest.raises(_lib.PkvdError) as e:
+        _plan(2, 4, 1, 128, 16, seq=[5, -1])
+    assert e.value.code == _lib.PKVD_EINVAL
+
+
+def test_plan_identity_includes_batch_and_lengths(L):
+    # Two specs that differ only in batch (or only in lengths) must lay out
+    # different work: the plan is a value of every shape field.
+    a, ia = _plan(4, 8, 2, 128, 16, seq=[2048] * 4)
+    b, ib = _plan(6, 8, 2, 128, 16, seq=[256, 512, 768, 1024, 1536, 2048])
+    assert ia != ib and a["num_partial_rows"] != b["num_partial_rows"]
+    c, ic = _plan(4, 8, 2, 128, 16, seq=[2048, 2048, 2048, 2047])
+    assert ic != ia
+
+
+def test_empty_batch_entries(L):
+    info, items = _plan(3, 4, 1, 128, 16, seq=[0, 0, 0])
+    assert info["num_items"] == 0 and info["num_partial_rows"] == 0
+    info, items = _plan(3, 4, 1, 128, 16, seq=[0, 33, 0])
+    assert all(it[0] == 1 for it in items)
