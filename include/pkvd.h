@@ -206,6 +206,28 @@ int decode_last_device_status(const pkvd_plan *plan, pkvd_stream_t stream);
 int decode_plan_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
                         pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
 
+/* A decode op that allocates no device memory. The paper has no counterpart
+ * to this call. It is for callers that cannot call cudaMalloc: a host
+ * application that owns all device memory through its own pool, or code that
+ * runs where allocating is forbidden or would stall the stream. It plans on
+ * the host like decode_plan_ex (same desc and seq_lens rules) and launches
+ * the same kernels, but keeps all scratch (status word, split table, work
+ * list, split partials) in one static 16 MiB device array that the library
+ * holds on every device that loads it until the process exits.
+ *   - The scratch a call needs must fit 16 MiB (about rows * heads * (Dv + 1)
+ *     * 4 bytes for the partials); larger problems return PKVD_ENOMEM and
+ *     queue nothing.
+ *   - All calls share the array: calls on one stream run in order, calls that
+ *     overlap on the GPU (other streams, unsynchronised threads) race.
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make it before any stream capture.
+ *   - Device-side page-id checks and wait timeouts are not reported.
+ * q, k_pages, v_pages, page_table, out and lse are as for decode_run;
+ * desc and seq_lens are host pointers, read during the call only. */
+int decode_run_static(const pkvd_plan_desc *desc, const int32_t *seq_lens, const void *q,
+                      const void *k_pages, const void *v_pages, const int32_t *page_table,
+                      float *out, float *lse, pkvd_stream_t stream);
+
 /* Static description of a status code. */
 const char *decode_status_string(int status);
 

@@ -69,6 +69,8 @@ SIGNATURES = {
     "decode_plan_compute": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp,
                                            ctypes.POINTER(PlanInfo), _vp, _i64]),
     "decode_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _vp]),
 }
 
 _lock = threading.Lock()
