@@ -145,6 +145,10 @@ typedef struct pkvd_plan_info {
   int32_t pipeline_stages;    /* shared-memory stages of the stage-1 kernel       */
   int32_t stage1_smem_bytes;  /* dynamic shared memory of a stage-1 block         */
   int32_t stage1_threads;     /* threads of a stage-1 block                       */
+  int32_t kv_tiles;           /* 1: K/V pages move as whole 16-row TMA tiles
+                                 (page size a multiple of 16, splits on 16-token
+                                 boundaries); 0: one bulk copy per row            */
+  int32_t reserved_info;
 } pkvd_plan_info;
 
 /* One stage-1 work item as the planner lays it out (decode_plan_compute). */

@@ -41,7 +41,8 @@ class PlanInfo(ctypes.Structure):
         "num_partial_rows", "max_splits")] + [
         ("chunk", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)] + [
         (n, ctypes.c_int32) for n in ("block_tokens", "pipeline_stages",
-                                      "stage1_smem_bytes", "stage1_threads")]
+                                      "stage1_smem_bytes", "stage1_threads", "kv_tiles",
+                                      "reserved_info")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/pkvd.h"
@@ -25,20 +26,16 @@ struct pkvd_plan {
   pkvd::KernelEntry s2;
   int s2_smem = 0;
   float scale_log2 = 0.f;
+  // K/V tensor maps of the page-tile path, re-encoded when the pools move
+  mutable std::mutex maps_mutex;
+  mutable const void* maps_k = nullptr;
+  mutable const void* maps_v = nullptr;
+  mutable pkvd::KvTensorMaps maps{};
 };
 
 namespace {
 
 constexpr double kLog2e = 1.4426950408889634074;
-
-bool kernel_for(int variant, int dtype, int head_dim, int group, pkvd::KernelEntry* e) {
-  switch (variant) {
-    case PKVD_VARIANT_GQA_FMA: return pkvd::gqa_fma_kernel(dtype, head_dim, group, e);
-    case PKVD_VARIANT_GQA_MMA: return pkvd::gqa_mma_kernel(dtype, head_dim, group, e);
-    case PKVD_VARIANT_MLA_MMA: return pkvd::mla_mma_kernel(dtype, e);
-    default: return false;
-  }
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -58,6 +55,17 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
   if (cudaGetDevice(&cur) != cudaSuccess) return PKVD_ECUDA;
   if (cur != p->device) return PKVD_EINVAL;
 
+  pkvd::KvTensorMaps maps{};
+  if (any_work && p->s1.tiles) {
+    std::lock_guard<std::mutex> lock(p->maps_mutex);
+    if (p->maps_k != k || p->maps_v != v) {
+      const int rc = pkvd::encode_kv_maps(d, k, v, &p->maps);
+      if (rc != PKVD_OK) return rc;
+      p->maps_k = k;
+      p->maps_v = v;
+    }
+    maps = p->maps;
+  }
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return PKVD_ECUDA;
   if (any_work) {
     pkvd::Stage1Args a{};
@@ -79,7 +87,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
     a.dv = d.head_dim_v;
     a.scale_log2 = p->scale_log2;
     a.checks = d.checks;
-    void* args[] = {&a};
+    void* args[] = {&a, &maps};
     if (cudaLaunchKernel(p->s1.func, dim3(L.info.num_items), dim3(p->s1.threads), args,
                          static_cast<size_t>(p->s1.smem), stream) != cudaSuccess)
       return PKVD_ECUDA;
@@ -145,8 +153,7 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
   pkvd::KernelEntry s1, s2;
-  const int group = d.heads / d.kv_heads;
-  if (!kernel_for(d.variant, d.dtype, d.head_dim, group, &s1)) return PKVD_EUNSUPPORTED;
+  if (!pkvd::stage1_kernel(d, pkvd::plan_uses_tiles(d, seq_lens), &s1)) return PKVD_EUNSUPPORTED;
   pkvd::stage2_kernel(&s2);
   if (d.num_sms == 0) {
     int sms = 0;
@@ -157,6 +164,11 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   if (cudaFuncSetAttribute(s1.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1.smem) !=
       cudaSuccess)
     return PKVD_ECUDA;
+  // Ask for the largest shared-memory carveout so that several stage-1
+  // blocks fit on an SM when their pipelines allow it.
+  cudaFuncSetAttribute(s1.func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaGetLastError();
   if (d.ctas_per_sm == 0) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, s1.func, s1.threads,
@@ -182,7 +194,13 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   p->s1 = s1;
   p->s2 = s2;
   const pkvd::PlanLayout& L = p->layout;
-  p->s2_smem = std::max(1, L.info.max_splits) * 4;
+  p->s2_smem = pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles,
+                                       L.info.max_splits);
+  if (cudaFuncSetAttribute(s2.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           p->s2_smem) != cudaSuccess) {
+    delete p;
+    return PKVD_ECUDA;
+  }
   p->scale_log2 = static_cast<float>(static_cast<double>(L.desc.scale) * kLog2e);
 
   // one device allocation, carved in 256-byte aligned pieces

@@ -13,7 +13,7 @@
 
 namespace pkvd {
 
-// Producer warp + consumer warps per stage-1 block.
+// MLA stage 1: consumer warps per block (plus one producer warp).
 constexpr int kConsumerWarps = 4;
 constexpr int kStage1Threads = (kConsumerWarps + 1) * 32;
 
@@ -28,21 +28,48 @@ constexpr int kRowPad = 16;
 // Mbarrier area at the front of dynamic shared memory.
 constexpr int kBarrierBytes = 256;
 
-// GQA: one stage = 16 tokens of K and 16 of V (one page at page size 16).
+// GQA stage 1: gqa_warps(D) warps per block. Each warp owns
+// gqa_stages_per_warp(D) shared-memory stages and issues the copies of its
+// own blocks: a warp's copies are issued one after another, so several
+// issuing warps keep many copies in flight, and a second stage per warp keeps
+// a copy in flight while the warp computes on the other.
+// One stage = 16 tokens of K and 16 of V (one page at page size 16), moved
+// either as two whole 16-row tiles through TMA tensor maps (128-byte swizzle,
+// tiles = true) or as one bulk copy per row into padded rows (tiles = false).
 constexpr int kGqaBlockTokens = 16;
-PKVD_HD constexpr int gqa_stages(int D) { return D == 256 ? 6 : 8; }
+constexpr int kTileAlign = 1024;    // swizzled tiles start on 1 KB boundaries
+PKVD_HD constexpr int gqa_warps(int) { return 6; }
+PKVD_HD constexpr int gqa_stages_per_warp(int D) { return D == 256 ? 1 : 2; }
+PKVD_HD constexpr int gqa_threads(int D) { return gqa_warps(D) * 32; }
+PKVD_HD constexpr int gqa_stages(int D) { return gqa_warps(D) * gqa_stages_per_warp(D); }
 PKVD_HD constexpr int gqa_row_pitch(int D) { return D * 2 + kRowPad; }
-PKVD_HD constexpr int gqa_stage_bytes(int D) { return 2 * kGqaBlockTokens * gqa_row_pitch(D); }
-// p values and rescale factors each consumer warp publishes per block
-PKVD_HD constexpr int gqa_pbuf_bytes(int G) {
-  return kConsumerWarps * (kGqaBlockTokens * G + G) * 4;
+PKVD_HD constexpr int gqa_tile_bytes(int D, bool tiles) {
+  return tiles ? kGqaBlockTokens * D * 2 : kGqaBlockTokens * gqa_row_pitch(D);
 }
-PKVD_HD constexpr int gqa_smem_bytes(int D, int G) {
-  return kBarrierBytes + gqa_stages(D) * gqa_stage_bytes(D) + gqa_pbuf_bytes(G < 8 ? 8 : G);
+PKVD_HD constexpr int gqa_stage_bytes(int D, bool tiles) { return 2 * gqa_tile_bytes(D, tiles); }
+// p values and rescale factors each warp publishes per block (FMA variant)
+PKVD_HD constexpr int gqa_pbuf_bytes(int D, int G) {
+  return gqa_warps(D) * (kGqaBlockTokens * (G < 8 ? 8 : G) + (G < 8 ? 8 : G)) * 4;
+}
+// the group's query rows, padded like K/V rows (MMA variant: ldmatrix source
+// of the Q^T fragments)
+PKVD_HD constexpr int gqa_qtile_bytes(int D, int G) {
+  return (G < 8 ? 8 : G) * gqa_row_pitch(D);
 }
 // cross-warp merge area, carved from the (by then idle) stage buffers
 PKVD_HD constexpr int gqa_merge_bytes(int D, int G) {
-  return kConsumerWarps * (G * D + 2 * G) * 4;
+  return gqa_warps(D) * (G * D + 2 * G) * 4;
+}
+// the stage area, large enough to hold the merge area afterwards
+PKVD_HD constexpr int gqa_stage_area_bytes(int D, int G, bool tiles) {
+  return gqa_stages(D) * gqa_stage_bytes(D, tiles) > gqa_merge_bytes(D, G)
+             ? gqa_stages(D) * gqa_stage_bytes(D, tiles)
+             : gqa_merge_bytes(D, G);
+}
+// [align slack][stage area][barriers][p buffers][query tile]
+PKVD_HD constexpr int gqa_smem_bytes(int D, int G, bool tiles) {
+  return kTileAlign + gqa_stage_area_bytes(D, G, tiles) + kBarrierBytes + gqa_pbuf_bytes(D, G) +
+         gqa_qtile_bytes(D, G);
 }
 
 // MLA: one stage = 64 latent rows of 576 (V = the first 512 of each row),
@@ -61,8 +88,13 @@ constexpr int kMlaRedBytes = 2 * kConsumerWarps * kMlaHeads * 4;         // 512 
 constexpr int kMlaSmemBytes = kBarrierBytes + kMlaStages * kMlaStageBytes + kMlaQBytes +
                               kMlaPBytes + kMlaRedBytes;
 
-// Stage 2 keeps one weight per split in shared memory.
+// Stage 2 keeps one weight per split and 16 group sums per float4 column of
+// its Dv slice in shared memory.
 constexpr int kMaxSplits = 8192;
+constexpr int kMergeThreads = 256;
+PKVD_HD constexpr int stage2_smem_bytes(int dv_slice, int max_splits) {
+  return 16 * (dv_slice / 4) * 16 + (max_splits < 1 ? 1 : max_splits) * 4;
+}
 
 // Usable shared memory per SM and per block on sm_103a.
 constexpr int kSmemPerSm = 233472;     // 228 KB

@@ -2,6 +2,8 @@
 // launcher and the kernel translation units.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (type only; the driver is reached through the runtime)
+
 #include <cstdint>
 
 #include "../../include/pkvd.h"
@@ -42,18 +44,35 @@ struct Stage2Args {
   int32_t tiles;                 // Dv slices (gridDim.y)
 };
 
+// Tensor maps of the K and V pools for the whole-page tile path (unused,
+// zero, for kernels that copy rows).
+struct alignas(64) KvTensorMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+
 struct KernelEntry {
-  const void* func = nullptr;    // __global__ symbol, launched with one Stage*Args
+  const void* func = nullptr;    // __global__ symbol: (Stage1Args, KvTensorMaps) for stage 1,
+                                 // (Stage2Args) for the merge
   int threads = 0;
   int smem = 0;                  // dynamic shared memory bytes
   int block_tokens = 0;
   int stages = 0;
+  bool tiles = false;            // K/V move as TMA page tiles (needs tensor maps)
 };
 
 // Lookups; false when the combination has no kernel.
-bool gqa_fma_kernel(int dtype, int head_dim, int group, KernelEntry* e);
-bool gqa_mma_kernel(int dtype, int head_dim, int group, KernelEntry* e);
+bool gqa_fma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
+bool gqa_mma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
 bool mla_mma_kernel(int dtype, KernelEntry* e);
 bool stage2_kernel(KernelEntry* e);
+
+// Stage-1 kernel for a normalised plan description (variant resolved).
+bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e);
+
+// Encode the K and V tensor maps of the page-tile path for the given pool
+// pointers: {64 columns, pool rows, D/64 column blocks}, box {64, 16, D/64},
+// 128-byte swizzle. Returns a pkvd_status.
+int encode_kv_maps(const pkvd_plan_desc& d, const void* k, const void* v, KvTensorMaps* out);
 
 }  // namespace pkvd

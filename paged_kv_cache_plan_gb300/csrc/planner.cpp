@@ -34,25 +34,35 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-bool variant_shape(int variant, int head_dim, int group, VariantShape* out) {
+bool variant_shape(int variant, int head_dim, int group, bool tiles, VariantShape* out) {
   switch (variant) {
     case PKVD_VARIANT_GQA_FMA:
       if ((head_dim != 128 && head_dim != 256) || !is_pow2(group) || group > 8) return false;
-      *out = {kGqaBlockTokens, gqa_stages(head_dim), kStage1Threads,
-              gqa_smem_bytes(head_dim, group)};
+      *out = {kGqaBlockTokens, gqa_stages(head_dim), gqa_threads(head_dim),
+              gqa_smem_bytes(head_dim, group, tiles)};
       return true;
     case PKVD_VARIANT_GQA_MMA:
       if ((head_dim != 128 && head_dim != 256) || group < 1 || group > 16) return false;
-      *out = {kGqaBlockTokens, gqa_stages(head_dim), kStage1Threads,
-              gqa_smem_bytes(head_dim, group > 8 ? 16 : 8)};
+      *out = {kGqaBlockTokens, gqa_stages(head_dim), gqa_threads(head_dim),
+              gqa_smem_bytes(head_dim, group > 8 ? 16 : 8, tiles)};
       return true;
     case PKVD_VARIANT_MLA_MMA:
-      if (head_dim != kMlaDk) return false;
+      if (head_dim != kMlaDk || tiles) return false;
       *out = {kMlaBlockTokens, kMlaStages, kStage1Threads, kMlaSmemBytes};
       return true;
     default:
       return false;
   }
+}
+
+bool plan_uses_tiles(const pkvd_plan_desc& d, const int32_t* seq_lens) {
+  if (d.head_dim == kMlaDk || d.page_size % kGqaBlockTokens != 0) return false;
+  if (d.splits > 0)
+    for (int b = 0; b < d.batch; ++b) {
+      const int64_t chunk = std::max<int64_t>(1, ceil_div(seq_lens[b], d.splits));
+      if (ceil_div(seq_lens[b], chunk) > 1 && chunk % kGqaBlockTokens != 0) return false;
+    }
+  return true;   // planner chunks are multiples of the 16-token block
 }
 
 int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_desc* out,
@@ -115,7 +125,7 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
       return PKVD_EUNSUPPORTED;
   }
   VariantShape vs;
-  if (!variant_shape(d.variant, d.head_dim, group, &vs)) return PKVD_EUNSUPPORTED;
+  if (!variant_shape(d.variant, d.head_dim, group, false, &vs)) return PKVD_EUNSUPPORTED;
   *out = d;
   *family = mla ? PKVD_FAMILY_MLA : PKVD_FAMILY_GQA;
   return PKVD_OK;
@@ -130,8 +140,9 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
 
   const int B = d.batch;
   const int group = d.heads / d.kv_heads;
+  const bool kv_tiles = plan_uses_tiles(d, seq_lens);
   VariantShape vs;
-  variant_shape(d.variant, d.head_dim, group, &vs);
+  variant_shape(d.variant, d.head_dim, group, kv_tiles, &vs);
   const int blk = vs.block_tokens;
 
   PlanLayout& P = *out;
@@ -158,6 +169,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   I.pipeline_stages = vs.stages;
   I.stage1_smem_bytes = vs.smem;
   I.stage1_threads = vs.threads;
+  I.kv_tiles = kv_tiles ? 1 : 0;
   const int units = I.units_per_request;
 
   // --- split sizes
@@ -248,8 +260,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
     return PKVD_EUNSUPPORTED;
   }
   I.stage2_tiles = tiles;
-  const int per_tile = dv / tiles;
-  I.stage2_threads = std::min(256, std::max(32, ((per_tile / 4 + 31) / 32) * 32));
+  I.stage2_threads = kMergeThreads;
 
   // --- workspace: items, split table, partial outputs and lse, status word
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };

@@ -26,7 +26,11 @@ struct VariantShape {
   int threads;
   int smem;
 };
-bool variant_shape(int variant, int head_dim, int group, VariantShape* out);
+bool variant_shape(int variant, int head_dim, int group, bool tiles, VariantShape* out);
+
+// Whether the GQA kernels can move K/V as whole 16-row page tiles: the page
+// size is a multiple of 16 and every split starts on a 16-token boundary.
+bool plan_uses_tiles(const pkvd_plan_desc& normalised, const int32_t* seq_lens);
 
 // Validate and normalise `in`; resolve the family and (if AUTO) the variant.
 int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_desc* out,

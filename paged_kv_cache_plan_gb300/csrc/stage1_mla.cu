@@ -25,11 +25,11 @@ namespace pkvd {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kPrefetchBlocks = 4;
+constexpr int kPrefetchBlocks = 6;
 
 template <typename T>
 __global__ void __launch_bounds__(kStage1Threads, 1)
-    mla_mma(const __grid_constant__ Stage1Args a) {
+    mla_mma(const __grid_constant__ Stage1Args a, const __grid_constant__ KvTensorMaps) {
   constexpr int BLK = kMlaBlockTokens;
   constexpr int STAGES = kMlaStages;
   constexpr int HB = kMlaHeads;
@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
       }
       return page;
     };
+    // Page ids of blocks j .. j + PF - 1 in a statically indexed register
+    // window (unrolled by PF): no register move waits on a pending load.
     int ids[PF][2];
 #pragma unroll
     for (int i = 0; i < PF; ++i) {
@@ -88,36 +90,37 @@ __global__ void __launch_bounds__(kStage1Threads, 1)
     }
     int j = 0;
     bool ok = true;
-    for (; j < nblk; ++j) {
-      const int p0 = ids[0][0], p1 = ids[0][1];
+    while (ok && j < nblk) {
 #pragma unroll
-      for (int i = 0; i < PF - 1; ++i) {
-        ids[i][0] = ids[i + 1][0];
-        ids[i][1] = ids[i + 1][1];
-      }
-      ids[PF - 1][0] = fetch(j + PF, lane);
-      ids[PF - 1][1] = fetch(j + PF, lane + 32);
-      const int s = j % STAGES;
-      if (j >= STAGES) {
-        bool freed = true;
-        if (lane == 0) freed = mbar_wait(bar_empty + 8 * s, ((j / STAGES) & 1) ^ 1);
-        if (!__shfl_sync(kFull, freed, 0)) {
-          ok = false;
-          break;
-        }
-      }
-      const int nv = min(BLK, n - j * BLK);
-      if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, static_cast<uint32_t>(nv * ROWB));
-      __syncwarp();
+      for (int i = 0; i < PF; ++i) {
+        if (j < nblk && ok) {
+          const int p0 = ids[i][0], p1 = ids[i][1];
+          ids[i][0] = fetch(j + PF, lane);
+          ids[i][1] = fetch(j + PF, lane + 32);
+          const int s = j % STAGES;
+          if (j >= STAGES) {
+            bool freed = true;
+            if (lane == 0) freed = mbar_wait(bar_empty + 8 * s, ((j / STAGES) & 1) ^ 1);
+            ok = __shfl_sync(kFull, freed, 0);
+          }
+          if (ok) {
+            const int nv = min(BLK, n - j * BLK);
+            if (lane == 0)
+              mbar_arrive_expect_tx(bar_full + 8 * s, static_cast<uint32_t>(nv * ROWB));
+            __syncwarp();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        if (r < nv) {
-          const int tok = it.tok_begin + j * BLK + r;
-          const int64_t row = (static_cast<int64_t>(h ? p1 : p0) * a.kv_heads) * a.page_size +
-                              tok % a.page_size;
-          bulk_copy_g2s(smem_addr(stages + s * SB + r * PITCH), pool + row * pitch_bytes, ROWB,
-                        bar_full + 8 * s);
+            for (int h = 0; h < 2; ++h) {
+              const int r = lane + 32 * h;
+              if (r < nv) {
+                const int tok = it.tok_begin + j * BLK + r;
+                const int64_t row = (static_cast<int64_t>(h ? p1 : p0) * a.kv_heads) *
+                                        a.page_size + tok % a.page_size;
+                bulk_copy_g2s(smem_addr(stages + s * SB + r * PITCH), pool + row * pitch_bytes,
+                              ROWB, bar_full + 8 * s);
+              }
+            }
+            ++j;
+          }
         }
       }
     }

@@ -10,8 +10,9 @@
 // the Dv output columns and re-derives M and sum_s w_s on its own, so the
 // slices never communicate -- the head-dim-tiled stage-2 reduce of the
 // aiter pull 4758 page (Technical Details 3). M and the weight sum are
-// always computed by warp 0 in the same lane-strided order, so every tiling
-// gives identical bits. The merge waits on stage 1 with griddepcontrol.wait,
+// always computed by warp 0 in the same lane-strided order, and the weighted
+// sums run over a fixed split-residue layout, so every tiling gives
+// identical bits. The merge waits on stage 1 with griddepcontrol.wait,
 // so it can be launched early (programmatic dependent launch).
 #include "device.cuh"
 #include "kernels.h"
@@ -20,33 +21,44 @@ namespace pkvd {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSplitGroups = 16;    // splits s = g, g + 16, g + 32, ... per group
+constexpr int kColThreads = 16;     // float4 columns per pass
+static_assert(kMergeThreads == kSplitGroups * kColThreads, "merge block shape");
 
-__global__ void __launch_bounds__(256) merge_splits(const __grid_constant__ Stage2Args a) {
-  extern __shared__ float w_s[];   // [S] weights
-  __shared__ float stats[2];       // M, sum of weights
+// Block layout: thread (g, c) = (tid / 16, tid % 16) sums, for each of its
+// float4 columns c, c + 16, ..., the weighted partials of splits s = g mod 16
+// in increasing s; the 16 group sums are then added in group order. The
+// order of every addition depends only on s and the column, never on the
+// tiling, so all tilings give identical bits.
+__global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_constant__ Stage2Args a) {
+  extern __shared__ float4 dyn[];   // [16][C4] group sums, then [S] weights
+  __shared__ float stats[2];        // M, sum of weights
 
   const int bh = blockIdx.x;
   const int b = bh / a.heads;
   const int h = bh - b * a.heads;
   const int dt = a.dv / a.tiles;
+  const int C4 = dt / 4;
   const int d0 = blockIdx.y * dt;
+  float4* gsum = dyn;
+  float* w_s = reinterpret_cast<float*>(dyn + kSplitGroups * C4);
 
   pdl_wait_prerequisites();
 
   const int r0 = a.split_base[b];
   const int S = a.split_base[b + 1] - r0;
-
+  for (int s = threadIdx.x; s < S; s += kMergeThreads)
+    w_s[s] = a.lse_part[static_cast<int64_t>(r0 + s) * a.heads + h];
+  __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     float m = -INFINITY;
-    for (int s = lane; s < S; s += 32)
-      m = fmaxf(m, a.lse_part[static_cast<int64_t>(r0 + s) * a.heads + h]);
+    for (int s = lane; s < S; s += 32) m = fmaxf(m, w_s[s]);
 #pragma unroll
     for (int x = 16; x >= 1; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
     float ws = 0.f;
     for (int s = lane; s < S; s += 32) {
-      const float l = a.lse_part[static_cast<int64_t>(r0 + s) * a.heads + h];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(l - m);
+      const float w = (m == -INFINITY) ? 0.f : exp2f(w_s[s] - m);
       w_s[s] = w;
       ws += w;
     }
@@ -63,36 +75,50 @@ __global__ void __launch_bounds__(256) merge_splits(const __grid_constant__ Stag
   const bool empty = (M == -INFINITY);
   const float inv = empty ? 0.f : 1.f / wsum;
 
-  const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv;
+  const int grp = threadIdx.x / kColThreads;
+  const int ct = threadIdx.x % kColThreads;
   const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
-  float* out = a.out + static_cast<int64_t>(bh) * a.dv;
-  for (int d = d0 + 4 * threadIdx.x; d < d0 + dt; d += 4 * blockDim.x) {
+  const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
+  for (int c = ct; c < C4; c += kColThreads) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
+    int s = grp;
+    for (; s + 3 * kSplitGroups < S; s += 4 * kSplitGroups) {
       float4 x[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        x[u] = __ldg(reinterpret_cast<const float4*>(base + (s + u) * stride + d));
+        x[u] = __ldg(reinterpret_cast<const float4*>(base + (s + u * kSplitGroups) * stride) + c);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float w = w_s[s + u];
+        const float w = w_s[s + u * kSplitGroups];
         acc.x = fmaf(w, x[u].x, acc.x);
         acc.y = fmaf(w, x[u].y, acc.y);
         acc.z = fmaf(w, x[u].z, acc.z);
         acc.w = fmaf(w, x[u].w, acc.w);
       }
     }
-    for (; s < S; ++s) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(base + s * stride + d));
+    for (; s < S; s += kSplitGroups) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(base + s * stride) + c);
       const float w = w_s[s];
       acc.x = fmaf(w, x.x, acc.x);
       acc.y = fmaf(w, x.y, acc.y);
       acc.z = fmaf(w, x.z, acc.z);
       acc.w = fmaf(w, x.w, acc.w);
     }
-    *reinterpret_cast<float4*>(out + d) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    gsum[grp * C4 + c] = acc;
+  }
+  __syncthreads();
+  float* out = a.out + static_cast<int64_t>(bh) * a.dv + d0;
+  for (int c = threadIdx.x; c < C4; c += kMergeThreads) {
+    float4 t = gsum[c];
+#pragma unroll
+    for (int g = 1; g < kSplitGroups; ++g) {
+      const float4 x = gsum[g * C4 + c];
+      t.x += x.x;
+      t.y += x.y;
+      t.z += x.z;
+      t.w += x.w;
+    }
+    reinterpret_cast<float4*>(out)[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
   }
   if (blockIdx.y == 0 && threadIdx.x == 0)
     a.lse[bh] = empty ? -INFINITY : (M + log2f(wsum)) * 0.69314718055994530942f;
@@ -102,8 +128,8 @@ __global__ void __launch_bounds__(256) merge_splits(const __grid_constant__ Stag
 
 bool stage2_kernel(KernelEntry* e) {
   e->func = reinterpret_cast<const void*>(&merge_splits);
-  e->threads = 0;   // chosen per plan
-  e->smem = 0;      // S floats, per plan
+  e->threads = kMergeThreads;
+  e->smem = 0;      // per plan: stage2_smem_bytes(Dv / tiles, max splits)
   return true;
 }
 

@@ -63,15 +63,6 @@ int scratch_address(int dev, unsigned char** out) {
 
 bool aligned16_static(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool stage1_kernel_for(int variant, int dtype, int head_dim, int group, pkvd::KernelEntry* e) {
-  switch (variant) {
-    case PKVD_VARIANT_GQA_FMA: return pkvd::gqa_fma_kernel(dtype, head_dim, group, e);
-    case PKVD_VARIANT_GQA_MMA: return pkvd::gqa_mma_kernel(dtype, head_dim, group, e);
-    case PKVD_VARIANT_MLA_MMA: return pkvd::mla_mma_kernel(dtype, e);
-    default: return false;
-  }
-}
-
 }  // namespace
 
 extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_lens,
@@ -88,8 +79,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
   pkvd::KernelEntry s1, s2;
-  if (!stage1_kernel_for(d.variant, d.dtype, d.head_dim, d.heads / d.kv_heads, &s1))
-    return PKVD_EUNSUPPORTED;
+  if (!pkvd::stage1_kernel(d, pkvd::plan_uses_tiles(d, seq_lens), &s1)) return PKVD_EUNSUPPORTED;
   pkvd::stage2_kernel(&s2);
   if (d.num_sms == 0 &&
       cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -97,6 +87,9 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   if (cudaFuncSetAttribute(s1.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1.smem) !=
       cudaSuccess)
     return PKVD_ECUDA;
+  cudaFuncSetAttribute(s1.func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaGetLastError();
   if (d.ctas_per_sm == 0) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, s1.func, s1.threads,
@@ -172,7 +165,12 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     a.dv = L.desc.head_dim_v;
     a.scale_log2 = static_cast<float>(static_cast<double>(L.desc.scale) * kLog2eStatic);
     a.checks = L.desc.checks;
-    void* args[] = {&a};
+    pkvd::KvTensorMaps maps{};
+    if (s1.tiles) {
+      rc = pkvd::encode_kv_maps(L.desc, k_pages, v_pages, &maps);
+      if (rc != PKVD_OK) return rc;
+    }
+    void* args[] = {&a, &maps};
     if (cudaLaunchKernel(s1.func, dim3(L.info.num_items), dim3(s1.threads), args,
                          static_cast<size_t>(s1.smem), stream) != cudaSuccess)
       return PKVD_ECUDA;
@@ -191,7 +189,11 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   cfg.gridDim = dim3(static_cast<unsigned>(L.desc.batch * L.desc.heads),
                      static_cast<unsigned>(m.tiles));
   cfg.blockDim = dim3(static_cast<unsigned>(L.info.stage2_threads));
-  cfg.dynamicSmemBytes = static_cast<size_t>(std::max(1, L.info.max_splits)) * 4;
+  cfg.dynamicSmemBytes = static_cast<size_t>(
+      pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles, L.info.max_splits));
+  if (cudaFuncSetAttribute(s2.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(cfg.dynamicSmemBytes)) != cudaSuccess)
+    return PKVD_ECUDA;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
