@@ -68,7 +68,7 @@ def peaks():
 def recorded_traffic(kernel_src: str, workload_name: str):
     """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         with open(path) as f:
             rec = json.load(f)

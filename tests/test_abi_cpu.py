@@ -121,9 +121,9 @@ def test_stage2_tiling_gate(L):
 
 
 def test_variant_resolution(L):
-    assert _plan(1, 16, 2, 256, 16, seq=[10])[0]["variant"] == 1      # FMA, group 8
+    assert _plan(1, 16, 2, 256, 16, seq=[10])[0]["variant"] == 2      # MMA by default
     assert _plan(1, 32, 2, 128, 16, seq=[10])[0]["variant"] == 2      # MMA, group 16
-    assert _plan(1, 16, 2, 256, 16, seq=[10], variant="gqa_mma")[0]["variant"] == 2
+    assert _plan(1, 16, 2, 256, 16, seq=[10], variant="gqa_fma")[0]["variant"] == 1
     assert _plan(1, 128, 1, 576, 1, seq=[10])[0]["variant"] == 3
     info = _plan(2, 128, 1, 576, 1, seq=[10, 20])[0]
     assert info["units_per_request"] == 8 and info["heads_per_unit"] == 16
@@ -141,7 +141,7 @@ def test_variant_resolution(L):
     (dict(args=(1, 4, 1, 128, 16), k_row_pitch=100), _lib.PKVD_EINVAL),   # pitch < D
     (dict(args=(1, 4, 1, 128, 16), k_row_pitch=132), _lib.PKVD_EINVAL),   # 264 B not 16-B aligned
     (dict(args=(1, 4, 1, 128, 16), max_pages_per_seq=3), _lib.PKVD_EINVAL),
-    (dict(args=(1, 32, 1, 128, 16), variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),
+    (dict(args=(1, 32, 1, 128, 16), variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),   # group 32
     (dict(args=(1, 4, 1, 128, 16), variant="mla_mma"), _lib.PKVD_EUNSUPPORTED),
 ])
 def test_argument_errors(L, kw, code):
