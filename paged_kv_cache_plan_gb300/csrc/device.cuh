@@ -1,6 +1,6 @@
 // Device-side building blocks for the sm_103a kernels: mbarrier pipeline
 // waits (bounded), bulk async copies global -> shared, warp-level tensor-core
-// fragments (ldmatrix / mma.sync / movmatrix), named barriers, programmatic
+// fragments (ldmatrix / mma.sync / movmatrix), programmatic
 // dependent launch, and the 16-bit <-> fp32 conversions.
 #pragma once
 
@@ -23,6 +23,12 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Two adjacent 16-bit values through the read-only path.
+template <typename T>
+__device__ __forceinline__ uint32_t ldg_pair(const T* p) {
+  return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {
@@ -113,27 +119,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t c0,
 // async-proxy (TMA) accesses of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// ------------------------------------------------------------ barriers
-
-// Named barrier over the consumer warps only (the producer never joins).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
-
-// Consumer barrier that also ORs a flag across all consumer threads.
-__device__ __forceinline__ bool consumer_sync_or(bool flag) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"(static_cast<uint32_t>(flag)), "n"(kConsumerWarps * 32)
-      : "memory");
-  return out != 0;
 }
 
 // ------------------------------------------- programmatic dependent launch

@@ -13,10 +13,6 @@
 
 namespace pkvd {
 
-// MLA stage 1: consumer warps per block (plus one producer warp).
-constexpr int kConsumerWarps = 4;
-constexpr int kStage1Threads = (kConsumerWarps + 1) * 32;
-
 // Every K/V row lands in shared memory at a pitch 16 bytes wider than the
 // row. Consecutive rows then start in different 16-byte bank groups, so the
 // 8 rows an ldmatrix (or a quarter-warp of 128-bit loads) touches hit 8
@@ -72,21 +68,23 @@ PKVD_HD constexpr int gqa_smem_bytes(int D, int G, bool tiles) {
          gqa_qtile_bytes(D, G);
 }
 
-// MLA: one stage = 64 latent rows of 576 (V = the first 512 of each row),
-// a block of 16 heads per work item.
-constexpr int kMlaBlockTokens = 64;
-constexpr int kMlaStages = 2;
+// MLA (mma.sync consumer): a block of 16 heads per work item, 4 warps, one
+// stage = 16 latent rows of 576 (V = the first 512 of each row) at the padded
+// pitch. Warp w scores the 16 keys of a block over dims 144w .. 144w+143 and
+// owns output columns 128w .. 128w+127; the four partial score tiles meet in
+// a double-buffered reduction area. Sized for two blocks per SM.
+constexpr int kMlaWarps = 4;
+constexpr int kMlaThreads = kMlaWarps * 32;
+constexpr int kMlaBlockTokens = 16;
+constexpr int kMlaStages = 5;
 constexpr int kMlaHeads = 16;
 constexpr int kMlaDk = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaRowPitch = kMlaDk * 2 + kRowPad;                       // 1168 B
-constexpr int kMlaStageBytes = kMlaBlockTokens * kMlaRowPitch;           // 74752 B
-constexpr int kMlaQBytes = kMlaHeads * kMlaRowPitch;                     // 18688 B
-constexpr int kMlaPPitch = (kMlaBlockTokens + 8) * 2;                    // 144 B
-constexpr int kMlaPBytes = 2 * kMlaHeads * kMlaPPitch;   // P high + low parts, 4608 B
-constexpr int kMlaRedBytes = 2 * kConsumerWarps * kMlaHeads * 4;         // 512 B
-constexpr int kMlaSmemBytes = kBarrierBytes + kMlaStages * kMlaStageBytes + kMlaQBytes +
-                              kMlaPBytes + kMlaRedBytes;
+constexpr int kMlaStageBytes = kMlaBlockTokens * kMlaRowPitch;           // 18688 B
+// partial scores: [2 buffers][4 warps][2 n-tiles][32 lanes] float4
+constexpr int kMlaRedBytes = 2 * kMlaWarps * 2 * 32 * 16;                // 8192 B
+constexpr int kMlaSmemBytes = kBarrierBytes + kMlaStages * kMlaStageBytes + kMlaRedBytes;
 
 // Stage 2 keeps one weight per split and 16 group sums per float4 column of
 // its Dv slice in shared memory.

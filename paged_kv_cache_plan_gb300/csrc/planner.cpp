@@ -48,7 +48,7 @@ bool variant_shape(int variant, int head_dim, int group, bool tiles, VariantShap
       return true;
     case PKVD_VARIANT_MLA_MMA:
       if (head_dim != kMlaDk || tiles) return false;
-      *out = {kMlaBlockTokens, kMlaStages, kStage1Threads, kMlaSmemBytes};
+      *out = {kMlaBlockTokens, kMlaStages, kMlaThreads, kMlaSmemBytes};
       return true;
     default:
       return false;
