@@ -393,7 +393,7 @@ def main():
                                     f"{case.batch} x {int(case.seq_lens[0])}"),
                        "kv_bytes_per_op": bytes_op,
                        "l2": "flushed before every step (512 MB write, then 512 MB read, outside the events)",
-                       "variant": ["auto", "gqa_fma", "gqa_mma", "mla_mma"][info["variant"]],
+                       "variant": {v: k for k, v in _lib.VARIANTS.items()}[info["variant"]],
                        "splits_max": info["max_splits"], "chunk": info["chunk"],
                        "work_items": info["num_items"], "ctas_per_sm": info["ctas_per_sm"],
                        "stage2_tiles": info["stage2_tiles"],

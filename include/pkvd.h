@@ -26,7 +26,7 @@
  *        {1, 2, 4, 8, 16}; K and V in separate pools.
  *   MLA  head_dim 576 (512 no-rope + 64 rope), head_dim_v 512, kv_heads 1,
  *        heads a multiple of 16; V is the first 512 elements of the same
- *        576-wide row (pass v_pages == k_pages, both row pitches 576).
+ *        576-wide row (pass v_pages == k_pages, both row pitches equal).
  *
  * Layouts (row-major, contiguous unless a pitch says otherwise):
  *   q          [batch, heads, head_dim]                   bf16 or fp16
@@ -86,7 +86,11 @@ typedef enum pkvd_variant {
   PKVD_VARIANT_AUTO = 0,
   PKVD_VARIANT_GQA_FMA = 1,   /* fp32 FMA scores and P.V, four keys per warp pass  */
   PKVD_VARIANT_GQA_MMA = 2,   /* mma.sync m16n8k16: keys as M, the head group as N */
-  PKVD_VARIANT_MLA_MMA = 3    /* mma.sync, a block of 16 heads per work item       */
+  PKVD_VARIANT_MLA_MMA = 3,   /* mma.sync, a block of 16 heads per work item       */
+  PKVD_VARIANT_MLA_TC = 4     /* tcgen05 with tensor-memory accumulators, a block
+                                 of 64 heads per work item (heads % 64 == 0); P
+                                 is rounded to one 16-bit value, so AUTO takes it
+                                 only when every request has >= 1024 tokens     */
 } pkvd_variant;
 
 /* Order of stage-1 work items in the grid. Both orders compute the same

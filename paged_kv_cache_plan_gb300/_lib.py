@@ -20,7 +20,7 @@ PKVD_OK, PKVD_EINVAL, PKVD_EUNSUPPORTED, PKVD_ECUDA = 0, -1, -2, -3
 PKVD_ENOMEM, PKVD_EDEVICE_CHECK, PKVD_ETIMEOUT = -4, -5, -6
 PKVD_BF16, PKVD_FP16 = 0, 1
 PKVD_FAMILY_GQA, PKVD_FAMILY_MLA = 0, 1
-VARIANTS = {"auto": 0, "gqa_fma": 1, "gqa_mma": 2, "mla_mma": 3}
+VARIANTS = {"auto": 0, "gqa_fma": 1, "gqa_mma": 2, "mla_mma": 3, "mla_tc": 4}
 GRID_ORDERS = {"auto": 0, "split_major": 1, "request_major": 2}
 
 

@@ -1,5 +1,6 @@
 // Device-side building blocks for the sm_103a kernels: mbarrier pipeline
-// waits (bounded), bulk async copies global -> shared, warp-level tensor-core
+// waits (bounded), bulk and per-thread async copies global -> shared, named
+// barriers, warp-level tensor-core
 // fragments (ldmatrix / mma.sync / movmatrix), programmatic
 // dependent launch, and the 16-bit <-> fp32 conversions.
 #pragma once
@@ -80,6 +81,69 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if ((i & 31u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
     if (i == 0x40000000u) return false;
   }
+}
+
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// ------------------------------------------------- per-thread async copies
+
+// One 16-byte global -> shared copy through the L1 path (any destination
+// layout), bypassing L1 on the way.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Hint: bring the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Close this thread's cp.async group; wait until at most N groups are pending.
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Named barrier `id` over `count` threads that also ORs a flag.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool flag) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(static_cast<uint32_t>(flag)), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------- bulk async copies

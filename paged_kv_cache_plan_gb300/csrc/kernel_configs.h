@@ -86,6 +86,31 @@ constexpr int kMlaStageBytes = kMlaBlockTokens * kMlaRowPitch;           // 1868
 constexpr int kMlaRedBytes = 2 * kMlaWarps * 2 * 32 * 16;                // 8192 B
 constexpr int kMlaSmemBytes = kBarrierBytes + kMlaStages * kMlaStageBytes + kMlaRedBytes;
 
+// MLA on the fifth-generation tensor cores (tcgen05): a block of 64 query
+// heads per work item, 64-key blocks in two stages. Warps 0-3 copy K/V rows
+// (16-byte cp.async chunks written straight into the 128-byte-swizzled
+// operand layout), warps 4-11 run the softmax, warp 12 issues the MMAs and
+// owns the tensor memory. Shared memory: [align slack][Q tile][2 stages]
+// [P tile][barriers and reduction scratch] = the whole 227 KB of a block.
+constexpr int kMlaTcHeads = 64;
+constexpr int kMlaTcBlockTokens = 64;
+constexpr int kMlaTcStages = 2;
+constexpr int kMlaTcLoadWarps = 4;
+constexpr int kMlaTcSoftmaxWarps = 8;
+constexpr int kMlaTcThreads = (kMlaTcLoadWarps + kMlaTcSoftmaxWarps + 1) * 32;   // 416
+constexpr int kMlaTcSlabBytes = kMlaTcBlockTokens * 128;     // 64 rows x 64 columns
+constexpr int kMlaTcStageBytes = (kMlaDk / 64) * kMlaTcSlabBytes;               // 73,728
+constexpr int kMlaTcQBytes = (kMlaDk / 64) * kMlaTcHeads * 128;                 // 73,728
+constexpr int kMlaTcPBytes = kMlaTcHeads * kMlaTcBlockTokens * 2;               // 8,192
+constexpr int kMlaTcMiscBytes = 2048;
+constexpr int kMlaTcSmemBytes = kTileAlign + kMlaTcQBytes + kMlaTcStages * kMlaTcStageBytes +
+                                kMlaTcPBytes + kMlaTcMiscBytes;                  // 232,448
+// The tcgen05 kernel rounds P to one 16-bit value (the mma.sync kernel keeps a
+// second, low part). AUTO uses it only when every request has at least this
+// many tokens, where the rounding errors of P average out far below the
+// output tolerance.
+constexpr int kMlaTcMinContext = 1024;
+
 // Stage 2 keeps one weight per split and 16 group sums per float4 column of
 // its Dv slice in shared memory.
 constexpr int kMaxSplits = 8192;

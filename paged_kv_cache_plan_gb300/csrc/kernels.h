@@ -46,7 +46,7 @@ struct Stage2Args {
 
 // Tensor maps of the K and V pools for the whole-page tile path (unused,
 // zero, for kernels that copy rows).
-struct alignas(64) KvTensorMaps {
+struct KvTensorMaps {
   CUtensorMap k;
   CUtensorMap v;
 };
@@ -65,6 +65,7 @@ struct KernelEntry {
 bool gqa_fma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
 bool gqa_mma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
 bool mla_mma_kernel(int dtype, KernelEntry* e);
+bool mla_tc_kernel(int dtype, KernelEntry* e);
 bool stage2_kernel(KernelEntry* e);
 
 // Stage-1 kernel for a normalised plan description (variant resolved).

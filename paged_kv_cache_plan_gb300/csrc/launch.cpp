@@ -19,6 +19,7 @@ bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e) {
     case PKVD_VARIANT_GQA_FMA: return gqa_fma_kernel(d.dtype, d.head_dim, group, tiles, e);
     case PKVD_VARIANT_GQA_MMA: return gqa_mma_kernel(d.dtype, d.head_dim, group, tiles, e);
     case PKVD_VARIANT_MLA_MMA: return !tiles && mla_mma_kernel(d.dtype, e);
+    case PKVD_VARIANT_MLA_TC: return !tiles && mla_tc_kernel(d.dtype, e);
     default: return false;
   }
 }

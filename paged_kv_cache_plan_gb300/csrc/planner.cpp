@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 
 #include "kernel_configs.h"
 
@@ -49,6 +50,10 @@ bool variant_shape(int variant, int head_dim, int group, bool tiles, VariantShap
     case PKVD_VARIANT_MLA_MMA:
       if (head_dim != kMlaDk || tiles) return false;
       *out = {kMlaBlockTokens, kMlaStages, kMlaThreads, kMlaSmemBytes};
+      return true;
+    case PKVD_VARIANT_MLA_TC:
+      if (head_dim != kMlaDk || tiles) return false;
+      *out = {kMlaTcBlockTokens, kMlaTcStages, kMlaTcThreads, kMlaTcSmemBytes};
       return true;
     default:
       return false;
@@ -116,8 +121,18 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
 
   const int group = d.heads / d.kv_heads;
   if (mla) {
-    if (d.variant == PKVD_VARIANT_AUTO) d.variant = PKVD_VARIANT_MLA_MMA;
-    if (d.variant != PKVD_VARIANT_MLA_MMA) return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_AUTO) {
+      // tensor-memory kernel for 64-head blocks over long contexts, where
+      // its one-part P rounding averages out (see kMlaTcMinContext)
+      int64_t min_len = INT64_MAX;
+      for (int b = 0; b < d.batch; ++b) min_len = std::min<int64_t>(min_len, seq_lens[b]);
+      d.variant = d.heads % kMlaTcHeads == 0 && min_len >= kMlaTcMinContext
+                      ? PKVD_VARIANT_MLA_TC
+                      : PKVD_VARIANT_MLA_MMA;
+    }
+    if (d.variant != PKVD_VARIANT_MLA_MMA && d.variant != PKVD_VARIANT_MLA_TC)
+      return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_MLA_TC && d.heads % kMlaTcHeads != 0) return PKVD_EUNSUPPORTED;
   } else {
     // The mma consumer is faster than the fp32 FMA consumer on every group
     // size measured on GB300 (the FMA path is issue-bound: about five
@@ -161,8 +176,8 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   I.num_sms = d.num_sms;
   I.ctas_per_sm = d.ctas_per_sm;
   if (family == PKVD_FAMILY_MLA) {
-    I.heads_per_unit = kMlaHeads;
-    I.units_per_request = d.heads / kMlaHeads;
+    I.heads_per_unit = d.variant == PKVD_VARIANT_MLA_TC ? kMlaTcHeads : kMlaHeads;
+    I.units_per_request = d.heads / I.heads_per_unit;
   } else {
     I.heads_per_unit = group;
     I.units_per_request = d.kv_heads;
@@ -200,7 +215,20 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
     // else one split per request
     const int64_t hi_c = std::max<int64_t>(min_chunk, ceil_div(std::max<int64_t>(maxL, 1), blk) * blk);
     int64_t C = hi_c;
-    if (items_for(hi_c) <= target) {
+    if (d.variant == PKVD_VARIANT_MLA_TC) {
+      // One resident block per SM and long items: choose the uniform split
+      // count that minimises waves x (tokens per item + a pipeline fill of
+      // two blocks), so that a last, partly filled wave costs little.
+      int64_t best = -1;
+      for (int64_t S = 1; S <= 64; ++S) {
+        const int64_t c = std::max<int64_t>(min_chunk, ceil_div(ceil_div(std::max<int64_t>(maxL, 1), S), blk) * blk);
+        const int64_t cost = ceil_div(items_for(c), target) * (c + 2 * blk);
+        if (best < 0 || cost < best) {
+          best = cost;
+          C = c;
+        }
+      }
+    } else if (items_for(hi_c) <= target) {
       int64_t lo = ceil_div(min_chunk, blk), hi = hi_c / blk;   // in blocks
       while (lo < hi) {
         const int64_t mid = (lo + hi) / 2;

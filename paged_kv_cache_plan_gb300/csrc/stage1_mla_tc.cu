@@ -1,0 +1,518 @@
+// Stage 1 for MLA on the fifth-generation tensor cores (tcgen05): one block
+// per work item (request b, block of 64 query heads, split s); all heads
+// share the 576-wide latent row of each token and V is its first 512
+// elements. This is the head-batched stage-1 of the aiter pull 4758 page
+// (Motivation, Technical Details 1) with the keys, not the heads, as the M
+// side of the products, because 64 heads x 512 fp32 output columns already
+// fill half of the tensor memory:
+//
+//   S^T [64 keys x 64 heads] = K [64 keys x 576] . Q^T              (M = 64)
+//   O^T [512 x 64 heads]    += V^T [512 x 64 keys] . P^T [64 keys x 64 heads]
+//                                                      (four M = 128 tiles)
+//
+// Tensor memory (512 columns): O^T tile t in columns 64t .. 64t+63, two S^T
+// buffers in columns 256 .. 383 (an M = 64 accumulator occupies lanes 0-15
+// of each 32-lane quarter: row i sits in lane 32 (i / 16) + i % 16), and the
+// softmax threads' running sums of P in columns 384 .. 447.
+//
+// Shared memory, all operands in the 128-byte-swizzled layout: the Q tile
+// (K-major, rows = heads), two K/V stages of nine 64-column slabs (one tile
+// serves as the K-major A operand of S^T and as the MN-major A operand of
+// O^T), and the P^T tile (MN-major, rows = keys). Shared memory holds only
+// two stages, so each stage is filled slab by slab with a barrier per slab:
+// the S^T products of a block start on its first slab while the later ones
+// are still arriving.
+//
+// Roles:
+//   warps 0-3   copy each block slab by slab as 16-byte cp.async chunks
+//               placed directly in the swizzled layout (one page per token
+//               leaves no contiguous tile to move); thread t copies rows
+//               t / 8 + 16 i (i < 4), chunk t % 8 of every slab; a slab's
+//               barrier completes when every copying thread's chunks of it
+//               have landed;
+//   warp 12     allocates the tensor memory; one thread issues the MMAs:
+//               O of a block as soon as its P is ready, the S^T products of
+//               the next block slab by slab as the slabs land (after a proxy
+//               fence: the copies wrote shared memory through the generic
+//               proxy, the tensor cores read it through the async proxy);
+//   warps 4-11  the softmax. Warp w reads the S^T lanes of quarter w % 4 (16
+//               keys) for 32 of the 64 heads. The running maximum per head is
+//               lazy: it is only raised when a block's scores exceed it by
+//               more than 2^8, so most blocks need no cross-warp reduction at
+//               all, only a vote; P = exp2(s - m) then lies below 2^8, which
+//               the 16-bit P and the fp32 sums absorb. When a head's maximum
+//               is raised, the block maxima are folded over lanes (transposing
+//               xor butterfly) and quarters (shared memory), and O^T and the
+//               running sums of that head are rescaled. P is rounded to one
+//               16-bit value.
+#include <type_traits>
+
+#include "device.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace pkvd {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLazyRescale = 8.f;   // log2 units
+constexpr int kSlabs = kMlaDk / 64;   // 9
+
+// Byte offset, in a tile of 64-column slabs of `slab_bytes` each, of 16-byte
+// chunk ch (0..71) of row r, 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz_off(int r, int ch, int slab_bytes) {
+  return (ch >> 3) * slab_bytes + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+// 2^x on the special-function unit (inputs here are <= 8 or -inf).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One step of the transposing xor butterfly: lanes with `up` keep the upper
+// N values, the others the lower N, each combined with its partner's copy.
+template <int N, bool MAX>
+__device__ __forceinline__ void fold_step(float* v, int offset, bool up) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float send = up ? v[i] : v[i + N];
+    const float keep = up ? v[i + N] : v[i];
+    const float got = __shfl_xor_sync(kFull, send, offset);
+    v[i] = MAX ? fmaxf(keep, got) : keep + got;
+  }
+}
+
+// Reduce 32 columns over the 16 lanes of each half-warp (max or sum, fixed
+// order); lane l ends with columns 2 (l % 16) and 2 (l % 16) + 1 in v[0..1].
+template <bool MAX>
+__device__ __forceinline__ void fold16(float (&v)[32], int lane) {
+  fold_step<16, MAX>(v, 8, lane & 8);
+  fold_step<8, MAX>(v, 4, lane & 4);
+  fold_step<4, MAX>(v, 2, lane & 2);
+  fold_step<2, MAX>(v, 1, lane & 1);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMlaTcThreads, 1)
+    mla_tc(const __grid_constant__ Stage1Args a, const __grid_constant__ KvTensorMaps) {
+  constexpr int R = kMlaTcHeads;              // 64 heads = N of both products
+  constexpr int BLK = kMlaTcBlockTokens;      // 64 keys
+  constexpr int SLAB = kMlaTcSlabBytes;       // one 64-column slab of 64 rows
+  constexpr int STAGE = kMlaTcStageBytes;
+  constexpr int CH = kMlaDk * 2 / 16;         // 72 16-byte chunks per row
+  constexpr int MMA_WARP = kMlaTcLoadWarps + kMlaTcSoftmaxWarps;
+  constexpr int LDT = kMlaTcLoadWarps * 32;   // copying threads
+  constexpr int SMX = kMlaTcSoftmaxWarps * 32;
+  constexpr int TCOLS = 512;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t kIdS = tc::idesc_f16(kBf16, BLK, R, false, false);
+  constexpr uint32_t kIdO = tc::idesc_f16(kBf16, 128, R, true, true);
+  static_assert(SLAB == R * 128, "the Q tile and the K/V stages share one slab size");
+  static_assert(4 * R + 2 * R + 64 <= TCOLS, "tensor memory columns");
+  static_assert(LDT == 2 * BLK && kMlaTcSoftmaxWarps == 8, "warp roles");
+
+  extern __shared__ uint8_t raw[];
+  uint8_t* sm = raw + ((kTileAlign - (smem_addr(raw) & (kTileAlign - 1))) & (kTileAlign - 1));
+  uint8_t* qs = sm;
+  uint8_t* stages = qs + kMlaTcQBytes;
+  uint8_t* ps = stages + kMlaTcStages * STAGE;
+  uint8_t* misc = ps + kMlaTcPBytes;
+  const uint32_t bars = smem_addr(misc);
+  const uint32_t full = bars;               // [2][9] slab landed (128 copying threads)
+  const uint32_t empty = bars + 144;        // [2] O of the stage's block done (MMA commit)
+  const uint32_t sfull = bars + 160;        // [2] S^T buffer written (MMA commit)
+  const uint32_t sfree = bars + 176;        // [2] S^T buffer read out (8 softmax warps)
+  const uint32_t pfull = bars + 192;        // P^T written, O rescaled if needed (8 warps)
+  const uint32_t odone = bars + 200;        // O of the latest block done (MMA commit)
+  const uint32_t drain = bars + 208;        // every issued MMA done (at exit)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  volatile int* resc_flag = reinterpret_cast<volatile int*>(misc + 264);   // [2]
+  float* m_ref = reinterpret_cast<float*>(misc + 512);      // [64] running maxima (log2)
+  float* alpha_s = reinterpret_cast<float*>(misc + 768);    // [64] rescale factors, then 1 / l
+  float* red = reinterpret_cast<float*>(misc + 1024);       // [4 quarters][64]
+  static_assert(1024 + 4 * 64 * 4 <= kMlaTcMiscBytes, "scratch area");
+
+  const pkvd_work_item it = a.items[blockIdx.x];
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = it.tok_end - it.tok_begin;
+  const int nblk = (n + BLK - 1) / BLK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      for (int c = 0; c < kSlabs; ++c) mbar_init(full + 8 * (s * kSlabs + c), LDT);
+      mbar_init(empty + 8 * s, 1);
+      mbar_init(sfull + 8 * s, 1);
+      mbar_init(sfree + 8 * s, kMlaTcSoftmaxWarps);
+    }
+    mbar_init(pfull, kMlaTcSoftmaxWarps);
+    mbar_init(odone, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // Q tile: the 64 heads as rows, K-major.
+  {
+    const uint8_t* qg = static_cast<const uint8_t*>(a.q) +
+                        (static_cast<int64_t>(it.request) * a.heads + it.unit * R) * (kMlaDk * 2);
+    for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
+      const int r = i / CH, ch = i - r * CH;
+      *reinterpret_cast<uint4*>(qs + swz_off(r, ch, SLAB)) =
+          __ldg(reinterpret_cast<const uint4*>(qg + r * (kMlaDk * 2)) + ch);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == MMA_WARP) tc::alloc(smem_addr(tslot), TCOLS);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp < kMlaTcLoadWarps) {
+    // ------------------------------------------------------------ copies
+    const int tid = threadIdx.x;
+    const int cq = tid & 7;                          // 16-byte chunk within a slab row
+    const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
+    const uint8_t* pool = static_cast<const uint8_t*>(a.k);
+    const int64_t pitch_bytes = a.k_pitch * 2;
+    // byte offset of the pool row of block row r of block j; rows past the
+    // item's end repeat its last row (their keys are masked)
+    auto row_off = [&](int j, int r) -> int64_t {
+      int tok = it.tok_begin + j * BLK + r;
+      if (tok >= it.tok_end) tok = it.tok_end - 1;
+      const int pidx = tok / a.page_size;
+      int page = __ldg(pt + pidx);
+      if (a.checks && (page < 0 || page >= a.num_pool_pages)) {
+        atomicOr(a.status, kStatusBadPage);
+        page = 0;
+      }
+      return (static_cast<int64_t>(page) * a.page_size + (tok - pidx * a.page_size)) *
+             pitch_bytes;
+    };
+    // this thread's rows of a block: tid / 8 + 16 i
+    int64_t cur[4], nxt[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cur[i] = nblk > 0 ? row_off(0, tid / 8 + 16 * i) : 0;
+    for (int j = 0; j < nblk; ++j) {
+      const int s = j & 1;
+      if (j >= 2) {
+        const bool ok = !*abort_flag && mbar_wait(empty + 8 * s, ((j >> 1) - 1) & 1);
+        if (!__all_sync(kFull, ok)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(a.status, kStatusTimeout);
+          }
+          break;
+        }
+      }
+      if (j + 1 < nblk) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) nxt[i] = row_off(j + 1, tid / 8 + 16 * i);
+      }
+      const uint32_t st = smem_addr(stages + s * STAGE);
+      // Each slab is announced asynchronously once this thread's copies of it
+      // have landed (cp.async arrive); the MMA thread fences them for the
+      // async proxy before its tensor-core reads.
+#pragma unroll 1
+      for (int c = 0; c < kSlabs; ++c) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          cp_async16(st + swz_off(tid / 8 + 16 * i, 8 * c + cq, SLAB),
+                     pool + cur[i] + (8 * c + cq) * 16);
+        cp_async_arrive(full + 8 * (s * kSlabs + c));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+    }
+    cp_async_wait_all();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0 && nblk > 0) {
+      // Descriptors are built once; a byte offset d within the first 256 KB
+      // of shared memory moves a descriptor by d / 16 in its start field, so
+      // every MMA below is one add and one issue (the single issuing thread
+      // is bound by its instruction latency, not by the tensor pipe).
+      const uint64_t dq = tc::sdesc(smem_addr(qs), 16, 1024);
+      const uint64_t dk0 = tc::sdesc(smem_addr(stages), 16, 1024);           // K-major
+      const uint64_t dv0 = tc::sdesc(smem_addr(stages), SLAB, 1024);         // MN-major
+      const uint64_t dp = tc::sdesc(smem_addr(ps), SLAB, 1024);
+      constexpr uint64_t kStageStep = STAGE >> 4, kSlabStep = SLAB >> 4;
+      int js = 0, cs = 0, jo = 0;   // next S^T block and slab, next O^T block
+      unsigned long long t0 = 0;
+      int idle = 0;
+      while (jo < nblk) {
+        bool progressed = false;
+        if (jo < js && mbar_test(pfull, jo & 1)) {
+          tc::fence_after();
+          const uint64_t dv = dv0 + (jo & 1) * kStageStep;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+#pragma unroll
+            for (int k = 0; k < BLK / 16; ++k)
+              tc::mma_f16(tbase + t * R, dv + t * 2 * kSlabStep + k * (2048 >> 4), dp + k * (2048 >> 4),
+                          kIdO, jo > 0 || k > 0);
+          tc::commit(empty + 8 * (jo & 1));
+          tc::commit(odone);
+          ++jo;
+          progressed = true;
+        }
+        // S^T of block js, one landed slab per pass (so that an O that
+        // became ready goes in between: MMA issue stalls while the pipe is full)
+        if (js < nblk && (cs > 0 || js < 2 || mbar_test(sfree + 8 * (js & 1), ((js >> 1) - 1) & 1)) &&
+            mbar_test(full + 8 * ((js & 1) * kSlabs + cs), (js >> 1) & 1)) {
+          fence_proxy_async_smem();   // the slab landed through the generic proxy
+          tc::fence_after();
+          const uint64_t off = cs * kSlabStep;
+          const uint64_t dk = dk0 + (js & 1) * kStageStep + off;
+          const uint32_t d = tbase + 4 * R + (js & 1) * R;
+          tc::mma_f16(d, dk, dq + off, kIdS, cs > 0);
+#pragma unroll
+          for (int k = 1; k < 4; ++k) tc::mma_f16(d, dk + 2 * k, dq + off + 2 * k, kIdS, true);
+          progressed = true;
+          if (++cs == kSlabs) {
+            tc::commit(sfull + 8 * (js & 1));
+            cs = 0;
+            ++js;
+          }
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle >= 64) {
+          // nothing to issue for a while: check the clock and the other roles
+          const unsigned long long now = global_timer_ns();
+          if (idle == 64) t0 = now;
+          if (*abort_flag || now - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(a.status, kStatusTimeout);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      // every issued MMA must be done before the tensor memory is freed
+      tc::commit(drain);
+      mbar_wait(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q = warp & 3;                         // tensor-memory lane quarter
+    const int h = (warp - kMlaTcLoadWarps) >> 2;    // heads 32h .. 32h+31
+    const int cl = lane & 15;
+    const int key = 16 * q + lane;                  // block key of this lane (lanes < 16)
+    const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
+    const bool decider = q == 0;                    // warps 4 and 8 finish the reductions
+    const float sl2 = a.scale_log2;
+    // running sums of P for this lane's key slot, per head, in the free
+    // tensor-memory columns 384 + 32h .. (registers are the scarce resource)
+    const uint32_t lcols = tbase + lanes + 6 * R + 32 * h;
+    // this lane's scaled scores of block j (keys past the end: -inf)
+    auto scores = [&](int j, int b, float (&x)[32]) {
+      uint32_t r[32];
+      tc::ld32(tbase + lanes + 4 * R + b * R + 32 * h, r);
+      const bool valid = lane < 16 && key < min(BLK, n - j * BLK);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = valid ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+    };
+    bool bad = false;
+
+    for (int j = 0; j < nblk; ++j) {
+      const int b = j & 1;
+      const bool ok = __all_sync(kFull, !*abort_flag && mbar_wait(sfull + 8 * b, (j >> 1) & 1));
+      float x[32];
+      bool need = j == 0;
+      if (ok) {
+        tc::fence_after();
+        scores(j, b, x);
+        if (j > 0) {
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + 32 * h + 4 * c4);
+            need |= x[4 * c4] > m4.x + kLazyRescale;
+            need |= x[4 * c4 + 1] > m4.y + kLazyRescale;
+            need |= x[4 * c4 + 2] > m4.z + kLazyRescale;
+            need |= x[4 * c4 + 3] > m4.w + kLazyRescale;
+          }
+        }
+      } else {
+        *abort_flag = 1;
+      }
+      // one vote per block: raise some maximum (or stop)
+      bool o_ready = false;
+      if (named_sync_or(1, SMX, need || !ok)) {
+        if (*abort_flag) {
+          bad = true;
+          break;
+        }
+        // -------- slow path: raise the reference maxima of the heads that need it
+        fold16<true>(x, lane);   // block maxima over this quarter's keys
+        if (lane < 16) {
+          red[q * 64 + 32 * h + 2 * cl] = x[0];
+          red[q * 64 + 32 * h + 2 * cl + 1] = x[1];
+        }
+        named_sync(1, SMX);
+        if (decider && lane < 16) {
+          bool raise = false;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 32 * h + 2 * cl + e;
+            const float bm =
+                fmaxf(fmaxf(red[col], red[64 + col]), fmaxf(red[128 + col], red[192 + col]));
+            const float mo = m_ref[col];
+            float mn = mo, al = 1.f;
+            if (j == 0) {
+              mn = bm;
+            } else if (bm > mo + kLazyRescale) {
+              mn = bm;
+              al = ex2(mo - mn);
+              raise = true;
+            }
+            m_ref[col] = mn;
+            alpha_s[col] = al;
+          }
+          const bool any = __any_sync(0x0000ffffu, raise);
+          if (lane == 0) resc_flag[h] = any ? 1 : 0;
+        }
+        named_sync(1, SMX);
+        if (resc_flag[0] | resc_flag[1]) {
+          // O of the previous block must be done before it is rescaled
+          if (!__all_sync(kFull, !*abort_flag && mbar_wait(odone, (j - 1) & 1))) *abort_flag = 1;
+          o_ready = true;
+          tc::fence_after();
+          // scale the O^T columns of this warp's heads (all four dv tiles,
+          // this quarter's lanes) and the running sums
+#pragma unroll 1
+          for (int t = 0; t < 5; ++t) {
+            const uint32_t cols = t < 4 ? tbase + lanes + t * R + 32 * h : lcols;
+            uint32_t o[32];
+            tc::ld32(cols, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha_s[32 * h + c]);
+            tc::st32(cols, o);
+          }
+          tc::wait_st();
+        }
+        scores(j, b, x);   // read again: the fold consumed the first copy
+      }
+      // S^T buffer b is in registers now
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree + 8 * b);
+      // O of the previous block must be done before P^T is rewritten (a wait
+      // that runs out stops the loop at the next vote)
+      if (j >= 1 && !o_ready && !__all_sync(kFull, !*abort_flag && mbar_wait(odone, (j - 1) & 1)))
+        *abort_flag = 1;
+      // P = exp2(s - m); P^T in the inputs' 16-bit type into shared memory
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(m_ref + 32 * h + 4 * c4);
+        x[4 * c4] = ex2(x[4 * c4] - m4.x);
+        x[4 * c4 + 1] = ex2(x[4 * c4 + 1] - m4.y);
+        x[4 * c4 + 2] = ex2(x[4 * c4 + 2] - m4.z);
+        x[4 * c4 + 3] = ex2(x[4 * c4 + 3] - m4.w);
+      }
+      if (lane < 16) {
+        uint8_t* prow = ps + (key >> 3) * 1024 + (key & 7) * 128;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(prow + (((4 * h + i) ^ (key & 7)) << 4)) = make_uint4(
+              pack2<T>(x[8 * i], x[8 * i + 1]), pack2<T>(x[8 * i + 2], x[8 * i + 3]),
+              pack2<T>(x[8 * i + 4], x[8 * i + 5]), pack2<T>(x[8 * i + 6], x[8 * i + 7]));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+      // running sums of P in fp32 (the log-sum-exp needs them unrounded)
+      {
+        tc::fence_after();
+        uint32_t l[32];
+        if (j > 0) tc::ld32(lcols, l);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          l[c] = __float_as_uint(j > 0 ? __uint_as_float(l[c]) + x[c] : x[c]);
+        tc::st32(lcols, l);
+        tc::wait_st();
+      }
+    }
+
+    if (!bad) {
+      const bool ok = __all_sync(
+          kFull, nblk == 0 || (!*abort_flag && mbar_wait(odone, (nblk - 1) & 1)));
+      float lp[32];
+      if (nblk > 0) {
+        uint32_t l[32];
+        tc::fence_after();
+        tc::ld32(lcols, l);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) lp[c] = __uint_as_float(l[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+      }
+      fold16<false>(lp, lane);   // sums over this quarter's keys
+      if (named_sync_or(1, SMX, !ok)) {
+        bad = true;
+      } else {
+        if (lane < 16) {
+          red[q * 64 + 32 * h + 2 * cl] = lp[0];
+          red[q * 64 + 32 * h + 2 * cl + 1] = lp[1];
+        }
+        named_sync(1, SMX);
+        const int64_t row0 = static_cast<int64_t>(it.partial_row) * a.heads + it.unit * R;
+        if (decider && lane < 16) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 32 * h + 2 * cl + e;
+            const float l = ((red[col] + red[64 + col]) + red[128 + col]) + red[192 + col];
+            alpha_s[col] = nblk > 0 ? 1.f / l : 0.f;
+            a.lse_part[row0 + col] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
+          }
+        }
+        named_sync(1, SMX);
+        tc::fence_after();
+#pragma unroll 1
+        for (int t = 0; t < 4; ++t) {
+          uint32_t o[32];
+          if (nblk > 0) {
+            tc::ld32(tbase + lanes + t * R + 32 * h, o);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+          }
+          float* orow = a.o_part + (row0 + 32 * h) * a.dv + 128 * t + 32 * q + lane;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) orow[c * a.dv] = __uint_as_float(o[c]) * alpha_s[32 * h + c];
+        }
+      }
+    }
+    if (bad && threadIdx.x == kMlaTcLoadWarps * 32) {
+      *abort_flag = 1;
+      atomicOr(a.status, kStatusTimeout);
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc::fence_after();
+    tc::dealloc(tbase, TCOLS);
+  }
+}
+
+}  // namespace
+
+bool mla_tc_kernel(int dtype, KernelEntry* e) {
+  e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_tc<__half>)
+                               : reinterpret_cast<const void*>(&mla_tc<__nv_bfloat16>);
+  e->threads = kMlaTcThreads;
+  e->smem = kMlaTcSmemBytes;
+  e->block_tokens = kMlaTcBlockTokens;
+  e->stages = kMlaTcStages;
+  return true;
+}
+
+}  // namespace pkvd

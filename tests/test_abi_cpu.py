@@ -127,6 +127,22 @@ def test_variant_resolution(L):
     assert _plan(1, 128, 1, 576, 1, seq=[10])[0]["variant"] == 3
     info = _plan(2, 128, 1, 576, 1, seq=[10, 20])[0]
     assert info["units_per_request"] == 8 and info["heads_per_unit"] == 16
+    # tensor-memory MLA kernel: 64-head blocks, only for long contexts by default
+    info = _plan(2, 128, 1, 576, 1, seq=[1024, 4096])[0]
+    assert info["variant"] == 4 and info["heads_per_unit"] == 64 and info["units_per_request"] == 2
+    assert info["block_tokens"] == 64 and info["stage1_threads"] == 416
+    assert _plan(2, 128, 1, 576, 1, seq=[1023, 4096])[0]["variant"] == 3
+    assert _plan(1, 48, 1, 576, 1, seq=[4096])[0]["variant"] == 3
+    assert _plan(1, 64, 1, 576, 1, seq=[100], variant="mla_tc")[0]["variant"] == 4
+
+
+def test_tensor_memory_split_choice(L):
+    # one resident block per SM: the split count minimises waves x (tokens + fill)
+    info, items = _plan(64, 64, 1, 576, 1, seq=[16384] * 64, variant="mla_tc")
+    waves = -(-info["num_items"] // 152)
+    assert info["chunk"] % 64 == 0
+    assert waves * (info["chunk"] + 128) <= 2 * (16384 + 128)   # better than one split per request
+    _check_cover(info, items, [16384] * 64, 1)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -143,6 +159,8 @@ def test_variant_resolution(L):
     (dict(args=(1, 4, 1, 128, 16), max_pages_per_seq=3), _lib.PKVD_EINVAL),
     (dict(args=(1, 32, 1, 128, 16), variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),   # group 32
     (dict(args=(1, 4, 1, 128, 16), variant="mla_mma"), _lib.PKVD_EUNSUPPORTED),
+    (dict(args=(1, 16, 1, 576, 1), variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),    # heads % 64
+    (dict(args=(1, 8, 2, 128, 16), variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),
 ])
 def test_argument_errors(L, kw, code):
     args = kw.pop("args")

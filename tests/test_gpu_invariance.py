@@ -25,6 +25,8 @@ def _cases():
                                seq_lens=[3000, 17, 900], pool_pages=400, seed=91), "gqa_mma"),
         "mla": (W.mla_case(batch=4, heads=16, seq_len=2000, prefix_len=1500, group=2,
                            pool_rows=8000, seed=92), "mla_mma"),
+        "mla_tc": (W.mla_case(batch=3, heads=64, seq_len=1700, prefix_len=1200, group=2,
+                              pool_rows=6000, seed=93), "mla_tc"),
     }
 
 
