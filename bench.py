@@ -257,6 +257,8 @@ def main():
     ap.add_argument("--splits", type=int, default=-1, help="-1 = the workload's own choice")
     ap.add_argument("--cpu-budget", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefix", action="store_true",
+                    help="plan shared-prefix workloads as independent requests")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -279,7 +281,9 @@ def main():
     kw = {"variant": args.variant}
     if args.splits >= 0:
         kw["splits"] = args.splits
-    plan = plan_for_case(case, **kw)
+    groups = [g for g in case.meta.get("prefix_group", []) if g >= 0]
+    shared_prefix = not args.no_prefix and any(groups.count(g) > 1 for g in set(groups))
+    plan = plan_for_case(case, shared_prefix=shared_prefix, **kw)
     out = torch.empty((case.batch, case.heads, case.head_dim_v), dtype=torch.float32,
                       device="cuda")
     lse = torch.empty((case.batch, case.heads), dtype=torch.float32, device="cuda")
@@ -396,6 +400,7 @@ def main():
                        "variant": {v: k for k, v in _lib.VARIANTS.items()}[info["variant"]],
                        "splits_max": info["max_splits"], "chunk": info["chunk"],
                        "work_items": info["num_items"], "ctas_per_sm": info["ctas_per_sm"],
+                       "shared_prefix_items": info["num_prefix_items"],
                        "stage2_tiles": info["stage2_tiles"],
                        "grid_order": ["auto", "split_major", "request_major"][info["grid_order"]],
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -409,7 +414,7 @@ def main():
             "e2e": {"value": round(bytes_op / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "us_per_op": round(ms_e2e * 1e3, 2), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": ((info["num_prefix_items"] > 0) + (info["num_items"] > 0) + 1) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "wall_s_timed_region": round(t_wall, 3),

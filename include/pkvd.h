@@ -152,7 +152,8 @@ typedef struct pkvd_plan_info {
   int32_t kv_tiles;           /* 1: K/V pages move as whole 16-row TMA tiles
                                  (page size a multiple of 16, splits on 16-token
                                  boundaries); 0: one bulk copy per row            */
-  int32_t reserved_info;
+  int32_t num_prefix_items;   /* shared-prefix plans: grouped prefix items, run
+                                 before the num_items per-request items; else 0  */
 } pkvd_plan_info;
 
 /* One stage-1 work item as the planner lays it out (decode_plan_compute). */
@@ -163,7 +164,12 @@ typedef struct pkvd_work_item {
   int32_t partial_row;        /* row of this split in the partial workspace      */
   int32_t tok_begin;          /* first logical token                              */
   int32_t tok_end;            /* one past the last logical token                 */
-  int32_t reserved0, reserved1;
+  int32_t grouped;            /* 1: a shared-prefix item: `request` is the first
+                                 of `unit` consecutive requests whose heads fill
+                                 the 64 query rows, `split` their prefix split,
+                                 partial_row unused (each member's row is its
+                                 first partial row + split); else 0              */
+  int32_t reserved1;
 } pkvd_work_item;
 
 /* GQA shorthand of decode_plan_ex (head_dim_v = head_dim, bf16, all other
@@ -176,6 +182,30 @@ int decode_plan(pkvd_plan **out, int batch, int heads, int kv_heads, int head_di
  * planner, allocates and fills the device work list and the partial
  * workspace. *out receives the plan (NULL on error). */
 int decode_plan_ex(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens);
+
+/* Shared-prefix plan (MLA only, heads in {16, 32, 64}). prefix_group[b] >= 0
+ * puts request b in a group; the members of a group must be consecutive
+ * requests with equal prefix_len[b] (1 <= prefix_len[b] <= seq_lens[b]) and
+ * page_table rows whose first ceil(prefix_len / page_size) entries name the
+ * same pages (the caller's promise: the shared tokens are read through the
+ * first member's row). prefix_group[b] < 0: no sharing. The
+ * shared tokens are read once per 64/heads members, with the members' query
+ * heads batched as the N side of the tensor-core products (64 rows); each
+ * request's private tokens run as usual, and the merge combines both kinds
+ * of partials. This is the aiter pull 4758 page's hope of L2 reuse under
+ * prefix sharing (Technical Details 2) made explicit. Results equal the
+ * plain plan's within the usual tolerance. desc->splits applies to the
+ * private tokens only. */
+int decode_plan_prefix(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens,
+                       const int32_t *prefix_group, const int32_t *prefix_len);
+
+/* Host-only planning of a shared-prefix plan (no CUDA call): the grouped
+ * prefix items come first in `items`, then the per-request items; capacity
+ * must cover info->num_prefix_items + info->num_items. desc->num_sms and
+ * desc->ctas_per_sm (of the per-request kernel) must be set. */
+int decode_plan_prefix_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
+                               const int32_t *prefix_group, const int32_t *prefix_len,
+                               pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
 
 /* Launch stage 1 and the merge on `stream`. q, k_pages, v_pages, page_table,
  * out and lse are device pointers laid out as above. Asynchronous. */

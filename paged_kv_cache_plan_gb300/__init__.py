@@ -7,8 +7,10 @@ script, the ctypes binding with the same entry-point names, and the seeded
 synthetic workload generator. Importing the package does not load the CUDA
 library; the first call does, and fails loudly if it is not built.
 """
-from .api import (Plan, decode_plan, decode_plan_compute, decode_plan_ex, decode_run,
-                  decode_run_timed, make_desc, plan_for_case, run_case)
+from .api import (Plan, decode_plan, decode_plan_compute, decode_plan_ex, decode_plan_prefix,
+                  decode_plan_prefix_compute, decode_run, decode_run_timed, make_desc,
+                  plan_for_case, run_case)
 
-__all__ = ["Plan", "decode_plan", "decode_plan_ex", "decode_run", "decode_run_timed",
-           "decode_plan_compute", "make_desc", "plan_for_case", "run_case"]
+__all__ = ["Plan", "decode_plan", "decode_plan_ex", "decode_plan_prefix", "decode_run",
+           "decode_run_timed", "decode_plan_compute", "decode_plan_prefix_compute", "make_desc",
+           "plan_for_case", "run_case"]

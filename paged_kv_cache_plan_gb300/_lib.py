@@ -42,7 +42,7 @@ class PlanInfo(ctypes.Structure):
         ("chunk", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)] + [
         (n, ctypes.c_int32) for n in ("block_tokens", "pipeline_stages",
                                       "stage1_smem_bytes", "stage1_threads", "kv_tiles",
-                                      "reserved_info")]
+                                      "num_prefix_items")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -51,7 +51,7 @@ class PlanInfo(ctypes.Structure):
 class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "request", "unit", "split", "partial_row", "tok_begin", "tok_end",
-        "reserved0", "reserved1")]
+        "grouped", "reserved1")]
 
 
 # Every function the header declares, with (restype, argtypes).
@@ -70,6 +70,9 @@ SIGNATURES = {
     "decode_plan_compute": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp,
                                            ctypes.POINTER(PlanInfo), _vp, _i64]),
     "decode_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "decode_plan_prefix": (ctypes.c_int, [_pp, ctypes.POINTER(PlanDesc), _vp, _vp, _vp]),
+    "decode_plan_prefix_compute": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp,
+                                                  ctypes.POINTER(PlanInfo), _vp, _i64]),
     "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
 }

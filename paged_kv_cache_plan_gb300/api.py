@@ -113,6 +113,44 @@ def decode_plan_compute(desc: PlanDesc, seq_lens: Sequence[int], with_items: boo
     return info.as_dict(), items
 
 
+def _i32_array(vals) -> ctypes.Array:
+    vals = [int(x) for x in (vals.tolist() if hasattr(vals, "tolist") else vals)]
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def decode_plan_prefix(desc: PlanDesc, seq_lens: Sequence[int], prefix_group: Sequence[int],
+                       prefix_len: Sequence[int]) -> Plan:
+    """Shared-prefix plan (MLA): consecutive requests with one prefix_group id
+    >= 0 share their first prefix_len tokens (same pages)."""
+    h = ctypes.c_void_p()
+    arrs = [_seq_array(seq_lens), _i32_array(prefix_group), _i32_array(prefix_len)]
+    check(_lib.lib().decode_plan_prefix(ctypes.byref(h), ctypes.byref(desc),
+                                        *[ctypes.cast(x, ctypes.c_void_p) for x in arrs]),
+          "decode_plan_prefix")
+    return Plan(h, desc)
+
+
+def decode_plan_prefix_compute(desc: PlanDesc, seq_lens: Sequence[int],
+                               prefix_group: Sequence[int], prefix_len: Sequence[int]):
+    """Host-only shared-prefix planning: (info dict, grouped prefix items,
+    per-request items); items as (request, unit, split, partial_row,
+    tok_begin, tok_end, grouped)."""
+    L = _lib.lib()
+    info = PlanInfo()
+    arrs = [_seq_array(seq_lens), _i32_array(prefix_group), _i32_array(prefix_len)]
+    ptrs = [ctypes.cast(x, ctypes.c_void_p) for x in arrs]
+    check(L.decode_plan_prefix_compute(ctypes.byref(desc), *ptrs, ctypes.byref(info), None, 0),
+          "decode_plan_prefix_compute")
+    n = info.num_prefix_items + info.num_items
+    arr = (WorkItem * max(1, n))()
+    check(L.decode_plan_prefix_compute(ctypes.byref(desc), *ptrs, ctypes.byref(info),
+                                       ctypes.cast(arr, ctypes.c_void_p), n),
+          "decode_plan_prefix_compute")
+    rows = [(w.request, w.unit, w.split, w.partial_row, w.tok_begin, w.tok_end, w.grouped)
+            for w in arr[:n]]
+    return info.as_dict(), rows[:info.num_prefix_items], rows[info.num_prefix_items:]
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -170,14 +208,19 @@ def decode_run_timed(plan: Plan, q, k_pages, v_pages, page_table, out, lse, ev_b
                                       ctypes.c_void_p(s), *ev), "decode_run_timed")
 
 
-def plan_for_case(case, **kw) -> Plan:
-    """Plan matching a workloads.DecodeCase (splits from the case unless given)."""
-    kw.setdefault("splits", case.splits)
-    return decode_plan(case.batch, case.heads, case.kv_heads, case.head_dim, case.page_size,
-                       case.seq_lens.tolist(), head_dim_v=case.head_dim_v, dtype=case.dtype,
-                       max_pages_per_seq=case.max_pages, num_pool_pages=case.pool_pages,
-                       k_row_pitch=case.k_row_pitch, v_row_pitch=case.v_row_pitch,
-                       scale=case.scale, **kw)
+def plan_for_case(case, *, shared_prefix: bool = False, **kw) -> Plan:
+    """Plan matching a workloads.DecodeCase (splits from the case unless
+    given). shared_prefix: use the case's prefix groups (decode_plan_prefix)."""
+    kw.setdefault("splits", 0 if shared_prefix else case.splits)
+    desc = make_desc(case.batch, case.heads, case.kv_heads, case.head_dim, case.page_size,
+                     head_dim_v=case.head_dim_v, dtype=case.dtype,
+                     max_pages_per_seq=case.max_pages, num_pool_pages=case.pool_pages,
+                     k_row_pitch=case.k_row_pitch, v_row_pitch=case.v_row_pitch,
+                     scale=case.scale, **kw)
+    if shared_prefix:
+        return decode_plan_prefix(desc, case.seq_lens.tolist(), case.meta["prefix_group"],
+                                  case.meta["prefix_len"])
+    return decode_plan_ex(desc, case.seq_lens.tolist())
 
 
 def run_case(plan: Plan, case_dev, out: Optional[torch.Tensor] = None,

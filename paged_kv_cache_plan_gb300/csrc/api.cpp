@@ -18,11 +18,13 @@ struct pkvd_plan {
   void* dmem = nullptr;
   size_t dbytes = 0;
   pkvd_work_item* d_items = nullptr;
+  pkvd_work_item* d_pitems = nullptr;   // grouped shared-prefix items, if any
   int32_t* d_split_base = nullptr;
   float* d_opart = nullptr;
   float* d_lpart = nullptr;
   int32_t* d_status = nullptr;
   pkvd::KernelEntry s1;
+  pkvd::KernelEntry s1p;                // kernel of the shared-prefix items
   pkvd::KernelEntry s2;
   int s2_smem = 0;
   float scale_log2 = 0.f;
@@ -45,7 +47,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
   if (!p || !out || !lse) return PKVD_EINVAL;
   const pkvd::PlanLayout& L = p->layout;
   const pkvd_plan_desc& d = L.desc;
-  const bool any_work = L.info.num_items > 0;
+  const bool any_work = L.info.num_items > 0 || L.info.num_prefix_items > 0;
   if (any_work && (!q || !k || !v || !page_table)) return PKVD_EINVAL;
   if (any_work && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(page_table)))
     return PKVD_EINVAL;
@@ -74,6 +76,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
     a.v = v;
     a.page_table = page_table;
     a.items = p->d_items;
+    a.split_base = p->d_split_base;
     a.o_part = p->d_opart;
     a.lse_part = p->d_lpart;
     a.status = p->d_status;
@@ -88,7 +91,16 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
     a.scale_log2 = p->scale_log2;
     a.checks = d.checks;
     void* args[] = {&a, &maps};
-    if (cudaLaunchKernel(p->s1.func, dim3(L.info.num_items), dim3(p->s1.threads), args,
+    if (L.info.num_prefix_items > 0) {
+      pkvd::Stage1Args ap = a;
+      ap.items = p->d_pitems;
+      void* pargs[] = {&ap, &maps};
+      if (cudaLaunchKernel(p->s1p.func, dim3(L.info.num_prefix_items), dim3(p->s1p.threads),
+                           pargs, static_cast<size_t>(p->s1p.smem), stream) != cudaSuccess)
+        return PKVD_ECUDA;
+    }
+    if (L.info.num_items > 0 &&
+        cudaLaunchKernel(p->s1.func, dim3(L.info.num_items), dim3(p->s1.threads), args,
                          static_cast<size_t>(p->s1.smem), stream) != cudaSuccess)
       return PKVD_ECUDA;
   }
@@ -142,7 +154,14 @@ int decode_plan_compute(const pkvd_plan_desc* desc, const int32_t* seq_lens,
   return PKVD_OK;
 }
 
-int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens) {
+}  // extern "C"
+
+namespace {
+
+// Plan creation shared by decode_plan_ex and decode_plan_prefix (prefix
+// arrays null for a plain plan).
+int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens,
+              const int32_t* prefix_group, const int32_t* prefix_len) {
   if (!out || !desc) return PKVD_EINVAL;
   *out = nullptr;
   pkvd_plan_desc d;
@@ -152,9 +171,17 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
-  pkvd::KernelEntry s1, s2;
-  if (!pkvd::stage1_kernel(d, pkvd::plan_uses_tiles(d, seq_lens), &s1)) return PKVD_EUNSUPPORTED;
+  const bool prefix = prefix_group != nullptr;
+  pkvd::KernelEntry s1, s1p, s2;
+  if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, seq_lens), &s1))
+    return PKVD_EUNSUPPORTED;
   pkvd::stage2_kernel(&s2);
+  if (prefix) {
+    if (family != PKVD_FAMILY_MLA || !pkvd::mla_tc_kernel(d.dtype, &s1p)) return PKVD_EUNSUPPORTED;
+    if (cudaFuncSetAttribute(s1p.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1p.smem) !=
+        cudaSuccess)
+      return PKVD_ECUDA;
+  }
   if (d.num_sms == 0) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -182,7 +209,8 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   pkvd_plan* p = new (std::nothrow) pkvd_plan;
   if (!p) return PKVD_ENOMEM;
   try {
-    rc = pkvd::plan_layout(d, seq_lens, &p->layout);
+    rc = prefix ? pkvd::plan_layout_prefix(d, seq_lens, prefix_group, prefix_len, &p->layout)
+                : pkvd::plan_layout(d, seq_lens, &p->layout);
   } catch (const std::bad_alloc&) {
     rc = PKVD_ENOMEM;
   }
@@ -192,6 +220,7 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   }
   p->device = dev;
   p->s1 = s1;
+  p->s1p = s1p;
   p->s2 = s2;
   const pkvd::PlanLayout& L = p->layout;
   p->s2_smem = pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles,
@@ -206,7 +235,8 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   // one device allocation, carved in 256-byte aligned pieces
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = static_cast<size_t>(std::max(1, L.info.num_partial_rows));
-  const size_t b_items = al(std::max<size_t>(L.items.size(), 1) * sizeof(pkvd_work_item));
+  const size_t n_items = L.items.size() + L.prefix_items.size();
+  const size_t b_items = al(std::max<size_t>(n_items, 1) * sizeof(pkvd_work_item));
   const size_t b_split = al(static_cast<size_t>(L.desc.batch + 1) * 4);
   const size_t b_opart = al(rows * L.desc.heads * L.desc.head_dim_v * 4);
   const size_t b_lpart = al(rows * L.desc.heads * 4);
@@ -219,6 +249,7 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   }
   char* base = static_cast<char*>(p->dmem);
   p->d_items = reinterpret_cast<pkvd_work_item*>(base);
+  p->d_pitems = p->d_items + L.items.size();
   p->d_split_base = reinterpret_cast<int32_t*>(base + b_items);
   p->d_opart = reinterpret_cast<float*>(base + b_items + b_split);
   p->d_lpart = reinterpret_cast<float*>(base + b_items + b_split + b_opart);
@@ -226,6 +257,10 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
   bool ok = true;
   if (!L.items.empty())
     ok = ok && cudaMemcpy(p->d_items, L.items.data(), L.items.size() * sizeof(pkvd_work_item),
+                          cudaMemcpyHostToDevice) == cudaSuccess;
+  if (!L.prefix_items.empty())
+    ok = ok && cudaMemcpy(p->d_pitems, L.prefix_items.data(),
+                          L.prefix_items.size() * sizeof(pkvd_work_item),
                           cudaMemcpyHostToDevice) == cudaSuccess;
   ok = ok && cudaMemcpy(p->d_split_base, L.split_base.data(), (L.desc.batch + 1) * 4,
                         cudaMemcpyHostToDevice) == cudaSuccess;
@@ -236,6 +271,43 @@ int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* s
     return PKVD_ECUDA;
   }
   *out = p;
+  return PKVD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int decode_plan_ex(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens) {
+  return make_plan(out, desc, seq_lens, nullptr, nullptr);
+}
+
+int decode_plan_prefix(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens,
+                       const int32_t* prefix_group, const int32_t* prefix_len) {
+  if (!prefix_group || !prefix_len) return PKVD_EINVAL;
+  return make_plan(out, desc, seq_lens, prefix_group, prefix_len);
+}
+
+int decode_plan_prefix_compute(const pkvd_plan_desc* desc, const int32_t* seq_lens,
+                               const int32_t* prefix_group, const int32_t* prefix_len,
+                               pkvd_plan_info* info, pkvd_work_item* items, int64_t capacity) {
+  if (!desc || !info) return PKVD_EINVAL;
+  pkvd::PlanLayout L;
+  int rc;
+  try {
+    rc = pkvd::plan_layout_prefix(*desc, seq_lens, prefix_group, prefix_len, &L);
+  } catch (const std::bad_alloc&) {
+    return PKVD_ENOMEM;
+  }
+  if (rc != PKVD_OK) return rc;
+  *info = L.info;
+  if (items) {
+    const size_t n = L.prefix_items.size() + L.items.size();
+    if (capacity < static_cast<int64_t>(n)) return PKVD_EINVAL;
+    std::memcpy(items, L.prefix_items.data(), L.prefix_items.size() * sizeof(pkvd_work_item));
+    std::memcpy(items + L.prefix_items.size(), L.items.data(),
+                L.items.size() * sizeof(pkvd_work_item));
+  }
   return PKVD_OK;
 }
 

@@ -17,6 +17,7 @@ struct Stage1Args {
   const void* v;                 // V pool, rows of v_pitch elements
   const int32_t* page_table;     // [B, pt_stride]
   const pkvd_work_item* items;   // [grid]
+  const int32_t* split_base;     // [B + 1] first partial row of each request (grouped items)
   float* o_part;                 // [rows, Hq, Dv] normalised partial outputs
   float* lse_part;               // [rows, Hq] partial log2-sum-exp2 (log2 domain)
   int32_t* status;               // device status word (kStatus* bits)

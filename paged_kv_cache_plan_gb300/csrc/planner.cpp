@@ -303,4 +303,130 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   return PKVD_OK;
 }
 
+int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
+                       const int32_t* prefix_group, const int32_t* prefix_len,
+                       PlanLayout* out) {
+  if (!prefix_group || !prefix_len || !seq_lens || in.batch < 1) return PKVD_EINVAL;
+  const int B = in.batch;
+  if (in.head_dim != kMlaDk) return PKVD_EUNSUPPORTED;
+  // normalise on the full lengths (page-table width, variant), then plan the
+  // private tokens with that description
+  pkvd_plan_desc nd;
+  int family = 0;
+  int nrc = normalise_desc(in, seq_lens, &nd, &family);
+  if (nrc != PKVD_OK) return nrc;
+  if (in.heads < 1 || kMlaTcHeads % in.heads != 0 || in.heads % kMlaHeads != 0)
+    return PKVD_EUNSUPPORTED;
+  const int per_unit = kMlaTcHeads / in.heads;   // requests whose heads fill 64 rows
+
+  // groups: runs of consecutive requests with one group id and prefix length
+  struct Group {
+    int first, count;
+    int64_t len;
+  };
+  std::vector<Group> groups;
+  std::vector<int32_t> plen(B, 0);
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0) return PKVD_EINVAL;
+    const int g = prefix_group[b];
+    if (g < 0) continue;
+    if (prefix_len[b] < 1 || prefix_len[b] > seq_lens[b]) return PKVD_EINVAL;
+    plen[b] = prefix_len[b];
+    if (b > 0 && prefix_group[b - 1] == g) {
+      if (prefix_len[b] != prefix_len[b - 1]) return PKVD_EINVAL;
+      ++groups.back().count;
+    } else {
+      for (const Group& o : groups)
+        if (prefix_group[o.first] == g) return PKVD_EINVAL;   // members not consecutive
+      groups.push_back({b, 1, prefix_len[b]});
+    }
+  }
+
+  // the private tokens: an ordinary plan on the suffix lengths
+  std::vector<int32_t> rest(B);
+  for (int b = 0; b < B; ++b) rest[b] = seq_lens[b] - plen[b];
+  int rc = plan_layout(nd, rest.data(), out);
+  if (rc != PKVD_OK) return rc;
+  PlanLayout& P = *out;
+  P.seq_lens.assign(seq_lens, seq_lens + B);
+
+  // prefix splits: one chunk for every group, chosen like the tensor-memory
+  // kernel's own splits (one resident block per SM)
+  constexpr int blk = kMlaTcBlockTokens;
+  const int64_t target = P.desc.num_sms;
+  auto items_for = [&](int64_t C) {
+    int64_t n = 0;
+    for (const Group& g : groups) n += ((g.count + per_unit - 1) / per_unit) * ceil_div(g.len, C);
+    return n;
+  };
+  int64_t maxp = 0;
+  for (const Group& g : groups) maxp = std::max(maxp, g.len);
+  int64_t Cp = std::max<int64_t>(blk, maxp);
+  if (!groups.empty()) {
+    int64_t best = -1;
+    for (int64_t S = 1; S <= 256; ++S) {
+      const int64_t c = std::max<int64_t>(2 * blk, ceil_div(ceil_div(maxp, S), blk) * blk);
+      const int64_t cost = ceil_div(items_for(c), target) * (c + 2 * blk);
+      if (best < 0 || cost < best) {
+        best = cost;
+        Cp = c;
+      }
+    }
+  }
+  std::vector<int32_t> sp(B, 0);   // prefix splits of each request
+  for (const Group& g : groups)
+    for (int m = 0; m < g.count; ++m) sp[g.first + m] = static_cast<int32_t>(ceil_div(g.len, Cp));
+
+  // partial rows of request b: its prefix splits, then its private splits
+  std::vector<int32_t> base(B + 1, 0);
+  int max_s = 0;
+  for (int b = 0; b < B; ++b) {
+    const int total = sp[b] + P.splits[b];
+    if (total > kMaxSplits) return PKVD_EUNSUPPORTED;
+    base[b + 1] = base[b] + total;
+    max_s = std::max(max_s, total);
+  }
+  for (pkvd_work_item& w : P.items) {
+    w.partial_row = base[w.request] + sp[w.request] + w.split;
+    w.tok_begin += plen[w.request];
+    w.tok_end += plen[w.request];
+  }
+  for (int b = 0; b < B; ++b) P.splits[b] = sp[b] + P.splits[b];
+  P.split_base = base;
+
+  // grouped prefix items, split-major so the units of one group run together
+  P.prefix_items.clear();
+  int64_t max_sp = 0;
+  for (const Group& g : groups) max_sp = std::max(max_sp, ceil_div(g.len, Cp));
+  for (int64_t s = 0; s < max_sp; ++s)
+    for (const Group& g : groups) {
+      if (s * Cp >= g.len) continue;
+      for (int u = 0; u * per_unit < g.count; ++u) {
+        pkvd_work_item w{};
+        w.request = g.first + u * per_unit;
+        w.unit = std::min(per_unit, g.count - u * per_unit);
+        w.split = static_cast<int32_t>(s);
+        w.partial_row = -1;
+        w.tok_begin = static_cast<int32_t>(s * Cp);
+        w.tok_end = static_cast<int32_t>(std::min<int64_t>(g.len, (s + 1) * Cp));
+        w.grouped = 1;
+        P.prefix_items.push_back(w);
+      }
+    }
+
+  pkvd_plan_info& I = P.info;
+  I.num_partial_rows = base[B];
+  I.max_splits = max_s;
+  I.num_prefix_items = static_cast<int32_t>(P.prefix_items.size());
+  I.chunk = 0;
+  auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t rows = std::max<int64_t>(I.num_partial_rows, 1);
+  const int64_t nitems = static_cast<int64_t>(P.items.size() + P.prefix_items.size());
+  I.workspace_bytes = al(std::max<int64_t>(nitems, 1) * static_cast<int64_t>(sizeof(pkvd_work_item))) +
+                      al(static_cast<int64_t>(B + 1) * 4) +
+                      al(rows * P.desc.heads * P.desc.head_dim_v * 4) + al(rows * P.desc.heads * 4) +
+                      al(16);
+  return PKVD_OK;
+}
+
 }  // namespace pkvd

@@ -16,6 +16,9 @@ struct PlanLayout {
   std::vector<int32_t> splits;       // S_b
   std::vector<int32_t> split_base;   // B + 1 prefix sums of S_b
   std::vector<pkvd_work_item> items; // stage-1 grid order
+  // Shared-prefix plans: grouped prefix items (tensor-memory MLA kernel),
+  // launched before `items`; empty otherwise.
+  std::vector<pkvd_work_item> prefix_items;
 };
 
 // Static per-variant numbers the planner needs (block tokens, stages,
@@ -38,5 +41,11 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
 
 // Full planning with desc->num_sms and desc->ctas_per_sm already set (> 0).
 int plan_layout(const pkvd_plan_desc& desc, const int32_t* seq_lens, PlanLayout* out);
+
+// Shared-prefix planning (see decode_plan_prefix): the per-request items of
+// the private tokens, planned as plan_layout does, plus grouped prefix items
+// for the tensor-memory MLA kernel (one resident block per SM).
+int plan_layout_prefix(const pkvd_plan_desc& desc, const int32_t* seq_lens,
+                       const int32_t* prefix_group, const int32_t* prefix_len, PlanLayout* out);
 
 }  // namespace pkvd

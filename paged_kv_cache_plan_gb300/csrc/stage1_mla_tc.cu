@@ -1,5 +1,8 @@
 // Stage 1 for MLA on the fifth-generation tensor cores (tcgen05): one block
-// per work item (request b, block of 64 query heads, split s); all heads
+// per work item (request b, block of 64 query heads, split s; or, for a
+// shared-prefix item, the heads of up to 64 / heads consecutive requests
+// over their common prefix, read through the first member's page table,
+// each head's partial going to its own request's partial row); all heads
 // share the 576-wide latent row of each token and V is its first 512
 // elements. This is the head-batched stage-1 of the aiter pull 4758 page
 // (Motivation, Technical Details 1) with the keys, not the heads, as the M
@@ -154,14 +157,32 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // Q tile: the 64 heads as rows, K-major.
+  // Query row r of the item: head unit * 64 + r of the request, or (grouped
+  // shared-prefix item) head r % heads of member r / heads; -1 for the unused
+  // rows of a group with fewer members than fit.
+  auto q_row = [&](int r) -> int64_t {
+    if (!it.grouped) return static_cast<int64_t>(it.request) * a.heads + it.unit * R + r;
+    const int m = r / a.heads;
+    return m < it.unit ? static_cast<int64_t>(it.request + m) * a.heads + (r - m * a.heads) : -1;
+  };
+  // Partial-output row of query row r (-1: unused).
+  auto out_row = [&](int r) -> int64_t {
+    if (!it.grouped) return static_cast<int64_t>(it.partial_row) * a.heads + it.unit * R + r;
+    const int m = r / a.heads;
+    return m < it.unit
+               ? static_cast<int64_t>(a.split_base[it.request + m] + it.split) * a.heads +
+                     (r - m * a.heads)
+               : -1;
+  };
+  // Q tile: the 64 query rows, K-major (unused rows zero).
   {
-    const uint8_t* qg = static_cast<const uint8_t*>(a.q) +
-                        (static_cast<int64_t>(it.request) * a.heads + it.unit * R) * (kMlaDk * 2);
     for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
       const int r = i / CH, ch = i - r * CH;
+      const int64_t qr = q_row(r);
       *reinterpret_cast<uint4*>(qs + swz_off(r, ch, SLAB)) =
-          __ldg(reinterpret_cast<const uint4*>(qg + r * (kMlaDk * 2)) + ch);
+          qr >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) +
+                                                         qr * (kMlaDk * 2)) + ch)
+                  : make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
   }
@@ -462,14 +483,14 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           red[q * 64 + 32 * h + 2 * cl + 1] = lp[1];
         }
         named_sync(1, SMX);
-        const int64_t row0 = static_cast<int64_t>(it.partial_row) * a.heads + it.unit * R;
         if (decider && lane < 16) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int col = 32 * h + 2 * cl + e;
             const float l = ((red[col] + red[64 + col]) + red[128 + col]) + red[192 + col];
             alpha_s[col] = nblk > 0 ? 1.f / l : 0.f;
-            a.lse_part[row0 + col] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
+            const int64_t orow = out_row(col);
+            if (orow >= 0) a.lse_part[orow] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
           }
         }
         named_sync(1, SMX);
@@ -483,9 +504,12 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = 0u;
           }
-          float* orow = a.o_part + (row0 + 32 * h) * a.dv + 128 * t + 32 * q + lane;
+          float* ocol = a.o_part + 128 * t + 32 * q + lane;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) orow[c * a.dv] = __uint_as_float(o[c]) * alpha_s[32 * h + c];
+          for (int c = 0; c < 32; ++c) {
+            const int64_t orow = out_row(32 * h + c);
+            if (orow >= 0) ocol[orow * a.dv] = __uint_as_float(o[c]) * alpha_s[32 * h + c];
+          }
         }
       }
     }

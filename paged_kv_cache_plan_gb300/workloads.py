@@ -173,10 +173,13 @@ def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
     vals = _randn((nxt, D), g, dtype)
     pool.view(R, D).index_copy_(0, used, vals)
     del vals
+    # shared-prefix description for decode_plan_prefix: consecutive groups
+    meta = {"prefix_group": [b // group if prefix_len > 0 else -1 for b in range(batch)],
+            "prefix_len": [prefix_len if prefix_len > 0 else 0] * batch}
     return DecodeCase(name, q, pool, pool, pt.to(torch.int32),
                       torch.full((batch,), seq_len, dtype=torch.int32), heads, 1, D, DV,
                       1, D, D, float(scale if scale is not None else 1.0 / math.sqrt(D)),
-                      dtype, True, splits, unique_rows=unique)
+                      dtype, True, splits, unique_rows=unique, meta=meta)
 
 
 # ---------------------------------------------------------------------------

@@ -190,3 +190,71 @@ def test_empty_batch_entries(L):
     assert info["num_items"] == 0 and info["num_partial_rows"] == 0
     info, items = _plan(3, 4, 1, 128, 16, seq=[0, 33, 0])
     assert all(it[0] == 1 for it in items)
+
+
+def _prefix_plan(B, heads, seq, groups, plen, **kw):
+    from paged_kv_cache_plan_gb300 import decode_plan_prefix_compute
+    kw.setdefault("num_sms", 152)
+    kw.setdefault("ctas_per_sm", 2)
+    return decode_plan_prefix_compute(make_desc(B, heads, 1, 576, 1, **kw), seq, groups, plen)
+
+
+def test_shared_prefix_plan_covers_every_token_once(L):
+    seq = [1000, 1000, 1000, 500, 800, 900, 64]
+    groups = [0, 0, 0, 1, 1, -1, 2]
+    plen = [700, 700, 700, 300, 300, 0, 64]
+    info, pre, rest = _prefix_plan(7, 16, seq, groups, plen)
+    assert info["num_prefix_items"] == len(pre) > 0 and info["num_items"] == len(rest)
+    assert all(g == 1 and 1 <= u <= 4 for (_, u, _, _, _, _, g) in pre)
+    assert all(g == 0 for (*_, g) in rest)
+    # members of a grouped item are the consecutive requests b .. b + unit - 1
+    cover = {b: [] for b in range(7)}
+    prefix_splits = {b: set() for b in range(7)}
+    for (b0, unit, s, _, t0, t1, _) in pre:
+        for b in range(b0, b0 + unit):
+            assert groups[b] == groups[b0] and t1 <= plen[b]
+            cover[b].append((t0, t1))
+            prefix_splits[b].add(s)
+    for (b, _, s, row, t0, t1, _) in rest:
+        assert t0 >= plen[b]
+        cover[b].append((t0, t1))
+    for b in range(7):
+        got = sorted(cover[b])
+        assert got[0][0] == 0 and got[-1][1] == seq[b]
+        for x, y in zip(got, got[1:]):
+            assert x[1] == y[0]
+        assert prefix_splits[b] == set(range(len(prefix_splits[b])))
+    # partial rows: each request's prefix splits, then its private splits
+    nrows = sum(len(prefix_splits[b]) for b in range(7)) + len(rest)
+    assert info["num_partial_rows"] == nrows
+    assert len({row for (_, _, _, row, _, _, _) in rest}) == len(rest)
+
+
+def test_shared_prefix_units_of_four_requests(L):
+    info, pre, rest = _prefix_plan(8, 16, [68000] * 8, [0] * 8, [63240] * 8)
+    units = {(b0, u) for (b0, u, *_) in pre}
+    assert units == {(0, 4), (4, 4)}
+    info, pre, _ = _prefix_plan(2, 32, [5000] * 2, [0] * 2, [4000] * 2)
+    assert {(b0, u) for (b0, u, *_) in pre} == {(0, 2)}
+
+
+@pytest.mark.parametrize("heads,groups,plen,seq,code", [
+    (16, [0, 1, 0], [10] * 3, [20] * 3, _lib.PKVD_EINVAL),        # members not consecutive
+    (16, [0, 0], [10, 11], [20, 20], _lib.PKVD_EINVAL),           # prefix lengths differ
+    (16, [0, 0], [21, 21], [20, 20], _lib.PKVD_EINVAL),           # longer than the request
+    (16, [0, 0], [0, 0], [20, 20], _lib.PKVD_EINVAL),             # empty prefix in a group
+    (128, [0, 0], [10, 10], [20, 20], _lib.PKVD_EUNSUPPORTED),    # 128 heads exceed 64 rows
+    (48, [0, 0], [10, 10], [20, 20], _lib.PKVD_EUNSUPPORTED),     # 48 does not divide 64
+])
+def test_shared_prefix_errors(L, heads, groups, plen, seq, code):
+    with pytest.raises(_lib.PkvdError) as e:
+        _prefix_plan(len(seq), heads, seq, groups, plen)
+    assert e.value.code == code
+
+
+def test_shared_prefix_needs_mla(L):
+    from paged_kv_cache_plan_gb300 import decode_plan_prefix_compute
+    with pytest.raises(_lib.PkvdError) as e:
+        decode_plan_prefix_compute(make_desc(2, 8, 2, 128, 16, num_sms=152, ctas_per_sm=1),
+                                   [32, 32], [0, 0], [16, 16])
+    assert e.value.code == _lib.PKVD_EUNSUPPORTED
