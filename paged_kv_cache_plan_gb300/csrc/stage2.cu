@@ -24,6 +24,7 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSplitGroups = 16;    // splits s = g, g + 16, g + 32, ... per group
 constexpr int kColThreads = 16;     // float4 columns per pass
 static_assert(kMergeThreads == kSplitGroups * kColThreads, "merge block shape");
+constexpr int kPre = 8;            // partials per thread loaded before the weights are known
 
 // Block layout: thread (g, c) = (tid / 16, tid % 16) sums, for each of its
 // float4 columns c, c + 16, ..., the weighted partials of splits s = g mod 16
@@ -47,6 +48,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
 
   const int r0 = a.split_base[b];
   const int S = a.split_base[b + 1] - r0;
+  const int grp = threadIdx.x / kColThreads;
+  const int ct = threadIdx.x % kColThreads;
+  const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
+  const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
+
+  // The first kPre partials of this thread's first column are loaded right
+  // away, in flight together with the split log-sum-exps: the weights need
+  // the lse values, the loads do not.
+  float4 pre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int s = grp + u * kSplitGroups;
+    pre[u] = ct < C4 && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + ct)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int s = threadIdx.x; s < S; s += kMergeThreads)
     w_s[s] = a.lse_part[static_cast<int64_t>(r0 + s) * a.heads + h];
   __syncthreads();
@@ -75,35 +91,30 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
   const bool empty = (M == -INFINITY);
   const float inv = empty ? 0.f : 1.f / wsum;
 
-  const int grp = threadIdx.x / kColThreads;
-  const int ct = threadIdx.x % kColThreads;
-  const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
-  const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
+  auto fma4 = [](float4& acc, float w, const float4& x) {
+    acc.x = fmaf(w, x.x, acc.x);
+    acc.y = fmaf(w, x.y, acc.y);
+    acc.z = fmaf(w, x.z, acc.z);
+    acc.w = fmaf(w, x.w, acc.w);
+  };
   for (int c = ct; c < C4; c += kColThreads) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = grp;
+    if (c == ct) {
+#pragma unroll
+      for (int u = 0; u < kPre; ++u, s += kSplitGroups)
+        if (s < S) fma4(acc, w_s[s], pre[u]);
+    }
     for (; s + 3 * kSplitGroups < S; s += 4 * kSplitGroups) {
       float4 x[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         x[u] = __ldg(reinterpret_cast<const float4*>(base + (s + u * kSplitGroups) * stride) + c);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = w_s[s + u * kSplitGroups];
-        acc.x = fmaf(w, x[u].x, acc.x);
-        acc.y = fmaf(w, x[u].y, acc.y);
-        acc.z = fmaf(w, x[u].z, acc.z);
-        acc.w = fmaf(w, x[u].w, acc.w);
-      }
+      for (int u = 0; u < 4; ++u) fma4(acc, w_s[s + u * kSplitGroups], x[u]);
     }
-    for (; s < S; s += kSplitGroups) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(base + s * stride) + c);
-      const float w = w_s[s];
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
-    }
+    for (; s < S; s += kSplitGroups)
+      fma4(acc, w_s[s], __ldg(reinterpret_cast<const float4*>(base + s * stride) + c));
     gsum[grp * C4 + c] = acc;
   }
   __syncthreads();
