@@ -370,8 +370,8 @@ def main():
 
     hbm, peak_src = peaks()
     achieved = bytes_op / (s1 * 1e-3) / 1e9
-    vname = {v: k for k, v in _lib.VARIANTS.items()}[info["variant"]]
-    if info["num_prefix_items"] > 0:
+    vname = {v: k for k, v in _lib.VARIANTS.items()}[plan.info["variant"]]
+    if plan.info["num_prefix_items"] > 0:
         vname = "mla_tc"   # the shared-prefix items dominate
     kernel_src = os.path.join(ROOT, "paged_kv_cache_plan_gb300", "csrc",
                               {"mla_tc": "stage1_mla_tc.cu", "mla_mma": "stage1_mla.cu"}.get(
