@@ -175,7 +175,6 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   pkvd::KernelEntry s1, s1p, s2;
   if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, seq_lens), &s1))
     return PKVD_EUNSUPPORTED;
-  pkvd::stage2_kernel(&s2);
   if (prefix) {
     if (family != PKVD_FAMILY_MLA || !pkvd::mla_tc_kernel(d.dtype, &s1p)) return PKVD_EUNSUPPORTED;
     if (cudaFuncSetAttribute(s1p.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1p.smem) !=
@@ -219,10 +218,14 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
     return rc;
   }
   p->device = dev;
+  const pkvd::PlanLayout& L = p->layout;
+  pkvd::stage2_kernel(pkvd::merge_prefers_deep(static_cast<int64_t>(L.desc.batch) * L.desc.heads *
+                                                   L.info.stage2_tiles,
+                                               L.desc.num_sms),
+                      &s2);
   p->s1 = s1;
   p->s1p = s1p;
   p->s2 = s2;
-  const pkvd::PlanLayout& L = p->layout;
   p->s2_smem = pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles,
                                        L.info.max_splits);
   if (cudaFuncSetAttribute(s2.func, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -67,7 +67,10 @@ bool gqa_fma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry*
 bool gqa_mma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
 bool mla_mma_kernel(int dtype, KernelEntry* e);
 bool mla_tc_kernel(int dtype, KernelEntry* e);
-bool stage2_kernel(KernelEntry* e);
+// deep_prefetch: the merge variant for small grids (see merge_splits).
+bool stage2_kernel(bool deep_prefetch, KernelEntry* e);
+// Whether a merge of `blocks` blocks on `num_sms` SMs takes the deep variant.
+inline bool merge_prefers_deep(int64_t blocks, int num_sms) { return blocks <= 2LL * num_sms; }
 
 // Stage-1 kernel for a normalised plan description (variant resolved).
 bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e);

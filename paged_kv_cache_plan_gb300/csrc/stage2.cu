@@ -24,13 +24,16 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSplitGroups = 16;    // splits s = g, g + 16, g + 32, ... per group
 constexpr int kColThreads = 16;     // float4 columns per pass
 static_assert(kMergeThreads == kSplitGroups * kColThreads, "merge block shape");
-constexpr int kPre = 8;            // partials per thread loaded before the weights are known
 
 // Block layout: thread (g, c) = (tid / 16, tid % 16) sums, for each of its
 // float4 columns c, c + 16, ..., the weighted partials of splits s = g mod 16
 // in increasing s; the 16 group sums are then added in group order. The
 // order of every addition depends only on s and the column, never on the
 // tiling, so all tilings give identical bits.
+// kPre: partials per thread loaded before the weights are known. Deep (8)
+// when the merge grid is small and latency-bound; shallow (2) when it is
+// large, where the extra registers would cost occupancy.
+template <int kPre>
 __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_constant__ Stage2Args a) {
   extern __shared__ float4 dyn[];   // [16][C4] group sums, then [S] weights
   __shared__ float stats[2];        // M, sum of weights
@@ -137,8 +140,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
 
 }  // namespace
 
-bool stage2_kernel(KernelEntry* e) {
-  e->func = reinterpret_cast<const void*>(&merge_splits);
+bool stage2_kernel(bool deep_prefetch, KernelEntry* e) {
+  e->func = deep_prefetch ? reinterpret_cast<const void*>(&merge_splits<8>)
+                          : reinterpret_cast<const void*>(&merge_splits<2>);
   e->threads = kMergeThreads;
   e->smem = 0;      // per plan: stage2_smem_bytes(Dv / tiles, max splits)
   return true;

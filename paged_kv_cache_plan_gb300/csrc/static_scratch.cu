@@ -80,7 +80,6 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
   pkvd::KernelEntry s1, s2;
   if (!pkvd::stage1_kernel(d, pkvd::plan_uses_tiles(d, seq_lens), &s1)) return PKVD_EUNSUPPORTED;
-  pkvd::stage2_kernel(&s2);
   if (d.num_sms == 0 &&
       cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKVD_ECUDA;
@@ -107,6 +106,10 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     return PKVD_ENOMEM;
   }
   if (rc != PKVD_OK) return rc;
+  pkvd::stage2_kernel(pkvd::merge_prefers_deep(static_cast<int64_t>(L.desc.batch) * L.desc.heads *
+                                                   L.info.stage2_tiles,
+                                               L.desc.num_sms),
+                      &s2);
   const bool any_work = L.info.num_items > 0;
   if (any_work && (!q || !k_pages || !v_pages || !page_table)) return PKVD_EINVAL;
   if (any_work && (!aligned16_static(q) || !aligned16_static(k_pages) ||
