@@ -79,6 +79,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
     a.split_base = p->d_split_base;
     a.o_part = p->d_opart;
     a.lse_part = p->d_lpart;
+    a.lse_stride = L.info.num_partial_rows;
     a.status = p->d_status;
     a.pt_stride = d.max_pages_per_seq;
     a.k_pitch = d.k_row_pitch;
@@ -109,6 +110,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
   pkvd::Stage2Args m{};
   m.o_part = p->d_opart;
   m.lse_part = p->d_lpart;
+  m.lse_stride = L.info.num_partial_rows;
   m.split_base = p->d_split_base;
   m.out = out;
   m.lse = lse;
@@ -219,15 +221,14 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   }
   p->device = dev;
   const pkvd::PlanLayout& L = p->layout;
-  pkvd::stage2_kernel(pkvd::merge_prefers_deep(static_cast<int64_t>(L.desc.batch) * L.desc.heads *
-                                                   L.info.stage2_tiles,
-                                               L.desc.num_sms),
-                      &s2);
+  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.heads, L.desc.head_dim_v, &s2)) {
+    delete p;   // the plan's merge shape and the kernel table disagree
+    return PKVD_EUNSUPPORTED;
+  }
   p->s1 = s1;
   p->s1p = s1p;
   p->s2 = s2;
-  p->s2_smem = pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles,
-                                       L.info.max_splits);
+  p->s2_smem = s2.smem;
   if (cudaFuncSetAttribute(s2.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            p->s2_smem) != cudaSuccess) {
     delete p;

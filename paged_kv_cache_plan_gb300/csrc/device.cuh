@@ -171,6 +171,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter, by its generic
+// address) into the descriptor cache ahead of its first copy.
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // Prefetch one tensor tile into L2 (no shared memory, no completion signal).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t c0, int32_t c1,
                                                    int32_t c2) {

@@ -52,9 +52,13 @@ PKVD_HD constexpr int gqa_pbuf_bytes(int D, int G) {
 PKVD_HD constexpr int gqa_qtile_bytes(int D, int G) {
   return (G < 8 ? 8 : G) * gqa_row_pitch(D);
 }
-// cross-warp merge area, carved from the (by then idle) stage buffers
+// cross-warp merge area, carved from the (by then idle) stage buffers:
+// [W][G] output rows of gqa_merge_row(D) floats (4 floats of padding, so the
+// quad lanes of an mma fragment, two heads apart, store to distinct banks),
+// then [W][G] maxima, [W][G] sums and [W][G] merge weights
+PKVD_HD constexpr int gqa_merge_row(int D) { return D + 4; }
 PKVD_HD constexpr int gqa_merge_bytes(int D, int G) {
-  return gqa_warps(D) * (G * D + 2 * G) * 4;
+  return gqa_warps(D) * (G * gqa_merge_row(D) + 3 * G) * 4;
 }
 // the stage area, large enough to hold the merge area afterwards
 PKVD_HD constexpr int gqa_stage_area_bytes(int D, int G, bool tiles) {
@@ -111,12 +115,26 @@ constexpr int kMlaTcSmemBytes = kTileAlign + kMlaTcQBytes + kMlaTcStages * kMlaT
 // output tolerance.
 constexpr int kMlaTcMinContext = 1024;
 
-// Stage 2 keeps one weight per split and 16 group sums per float4 column of
-// its Dv slice in shared memory.
+// Stage 2 keeps one float4 sum per warp (8 warps) and float4 column of its
+// Dv slice in shared memory.
 constexpr int kMaxSplits = 8192;
 constexpr int kMergeThreads = 256;
-PKVD_HD constexpr int stage2_smem_bytes(int dv_slice, int max_splits) {
-  return 16 * (dv_slice / 4) * 16 + (max_splits < 1 ? 1 : max_splits) * 4;
+PKVD_HD constexpr int stage2_smem_bytes(int dv_slice) {
+  return (kMergeThreads / 32) * (dv_slice / 4) * 16;
+}
+// With at most kMergeColMaxSplits splits per request the merge runs one
+// thread per float4 column instead (no shared memory), in blocks of
+// merge_col_threads(Dv slice) threads.
+constexpr int kMergeColMaxSplits = 8;
+PKVD_HD constexpr int merge_col_threads(int dv_slice) {
+  return ((dv_slice / 4 + 31) / 32) * 32 > 128 ? 128
+         : ((dv_slice / 4 + 31) / 32) * 32 < 32 ? 32
+                                                : ((dv_slice / 4 + 31) / 32) * 32;
+}
+// Threads per merge block for a plan whose requests have at most max_splits
+// splits, with Dv slices of dv_slice columns.
+PKVD_HD constexpr int merge_threads(int max_splits, int dv_slice) {
+  return max_splits <= kMergeColMaxSplits ? merge_col_threads(dv_slice) : kMergeThreads;
 }
 
 // Usable shared memory per SM and per block on sm_103a.

@@ -19,7 +19,9 @@ struct Stage1Args {
   const pkvd_work_item* items;   // [grid]
   const int32_t* split_base;     // [B + 1] first partial row of each request (grouped items)
   float* o_part;                 // [rows, Hq, Dv] normalised partial outputs
-  float* lse_part;               // [rows, Hq] partial log2-sum-exp2 (log2 domain)
+  float* lse_part;               // [Hq, lse_stride] partial log2-sum-exp2 (log2 domain),
+                                 // head-major: one head's splits are consecutive
+  int64_t lse_stride;            // partial rows of the plan
   int32_t* status;               // device status word (kStatus* bits)
   int64_t pt_stride;             // entries per page_table row
   int64_t k_pitch;               // elements between K rows
@@ -36,7 +38,8 @@ struct Stage1Args {
 // Arguments of the merge kernel (one block per (request, head, Dv slice)).
 struct Stage2Args {
   const float* o_part;
-  const float* lse_part;
+  const float* lse_part;         // [Hq, lse_stride]
+  int64_t lse_stride;
   const int32_t* split_base;     // [B + 1] first partial row of each request
   float* out;                    // [B, Hq, Dv]
   float* lse;                    // [B, Hq] natural log
@@ -67,10 +70,11 @@ bool gqa_fma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry*
 bool gqa_mma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
 bool mla_mma_kernel(int dtype, KernelEntry* e);
 bool mla_tc_kernel(int dtype, KernelEntry* e);
-// deep_prefetch: the merge variant for small grids (see merge_splits).
-bool stage2_kernel(bool deep_prefetch, KernelEntry* e);
-// Whether a merge of `blocks` blocks on `num_sms` SMs takes the deep variant.
-inline bool merge_prefers_deep(int64_t blocks, int num_sms) { return blocks <= 2LL * num_sms; }
+// The merge kernel of a plan (threads and shared memory filled in): one
+// thread per column when no request has more than kMergeColMaxSplits
+// splits; otherwise split-parallel, with deep prefetch when the merge grid
+// (batch x heads x Dv slices blocks) is at most two blocks per SM.
+bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, KernelEntry* e);
 
 // Stage-1 kernel for a normalised plan description (variant resolved).
 bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e);

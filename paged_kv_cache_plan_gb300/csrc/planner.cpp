@@ -290,7 +290,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
     return PKVD_EUNSUPPORTED;
   }
   I.stage2_tiles = tiles;
-  I.stage2_threads = kMergeThreads;
+  I.stage2_threads = merge_threads(max_s, dv / tiles);
 
   // --- workspace: items, split table, partial outputs and lse, status word
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
@@ -417,6 +417,7 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
   pkvd_plan_info& I = P.info;
   I.num_partial_rows = base[B];
   I.max_splits = max_s;
+  I.stage2_threads = merge_threads(max_s, P.desc.head_dim_v / I.stage2_tiles);
   I.num_prefix_items = static_cast<int32_t>(P.prefix_items.size());
   I.chunk = 0;
   auto al = [](int64_t x) { return (x + 255) / 256 * 256; };

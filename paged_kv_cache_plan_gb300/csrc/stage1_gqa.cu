@@ -118,22 +118,45 @@ __device__ __forceinline__ void prefetch_block(const KvTensorMaps& maps, int64_t
   }
 }
 
+// Pool rows of a warp's first blocks: the SPW blocks it copies first and
+// the PF blocks after them (the page-id window). Loaded at the very start of
+// the block, before the barrier set-up, so that the page-table round trip
+// overlaps it.
+template <int D, bool TILES>
+struct WarpRows {
+  static constexpr int SPW = gqa_stages_per_warp(D);
+  static constexpr int PF = 4;     // page-id window (blocks)
+  int64_t first[SPW];
+  int64_t rows[PF];
+  __device__ __forceinline__ WarpRows(const Stage1Args& a, const pkvd_work_item& it, int warp,
+                                      int lane) {
+    constexpr int W = gqa_warps(D);
+    const int n = it.tok_end - it.tok_begin;
+    const int nblk = (n + BLK - 1) / BLK;
+    const int r = TILES ? 0 : (lane & (BLK - 1));
+    const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
+#pragma unroll
+    for (int s = 0; s < SPW; ++s) first[s] = kv_row_of(a, it, pt, warp + W * s, nblk, r);
+#pragma unroll
+    for (int i = 0; i < PF; ++i) rows[i] = kv_row_of(a, it, pt, warp + W * (SPW + i), nblk, r);
+  }
+};
+
 // The per-warp pipeline: issue this warp's first SPW blocks, then for each of
 // its blocks wait, run `process(nv, stage)`, and refill the stage with the
 // block SPW further on. With TILES, the blocks PFL beyond the next refill are
-// also prefetched into L2, so that DRAM keeps streaming while a warp's single
-// stage is busy, even on items only a few blocks long per warp. Returns false
-// when a wait ran out (after waiting, bounded, for this warp's copies still in
-// flight). The caller's `prologue` runs once the first copies are in flight.
+// also prefetched into L2 (off: it did not pay). Returns false when a wait ran
+// out (after waiting, bounded, for this warp's copies still in flight). The
+// caller's `prologue` runs once the first copies are in flight.
 template <int D, bool TILES, typename P, typename F>
 __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTensorMaps& maps,
-                                              const pkvd_work_item& it, uint8_t* stages,
-                                              uint32_t bars, int warp, int lane, P&& prologue,
-                                              F&& process) {
+                                              const pkvd_work_item& it, WarpRows<D, TILES>& wr,
+                                              uint8_t* stages, uint32_t bars, int warp, int lane,
+                                              P&& prologue, F&& process) {
   constexpr int W = gqa_warps(D);
   constexpr int SPW = gqa_stages_per_warp(D);
   constexpr int SB = gqa_stage_bytes(D, TILES);
-  constexpr int PF = 4;               // page-id window (blocks)
+  constexpr int PF = WarpRows<D, TILES>::PF;
   constexpr int PFL = 0;              // L2 prefetch distance past the next refill (off)
   static_assert(PFL < PF, "prefetched rows come from the page-id window");
   const int n = it.tok_end - it.tok_begin;
@@ -144,17 +167,12 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
   auto blk_of = [&](int k) { return warp + W * k; };
   auto stage_of = [&](int k) { return stages + (warp * SPW + k % SPW) * SB; };
   auto bar_of = [&](int k) { return bars + 8u * (warp * SPW + k % SPW); };
+  int64_t (&rows)[PF] = wr.rows;
 
-  int64_t first[SPW];
-  int64_t rows[PF];
-#pragma unroll
-  for (int s = 0; s < SPW; ++s) first[s] = kv_row_of(a, it, pt, blk_of(s), nblk, r);
-#pragma unroll
-  for (int i = 0; i < PF; ++i) rows[i] = kv_row_of(a, it, pt, blk_of(SPW + i), nblk, r);
 #pragma unroll
   for (int s = 0; s < SPW; ++s)
     if (s < nmine)
-      issue_block<D, TILES>(a, maps, blk_of(s), n, first[s], stage_of(s), bar_of(s), lane);
+      issue_block<D, TILES>(a, maps, blk_of(s), n, wr.first[s], stage_of(s), bar_of(s), lane);
 #pragma unroll
   for (int i = 0; i < PFL; ++i)
     if (SPW + i < nmine) prefetch_block<D, TILES>(maps, rows[i], lane);
@@ -267,31 +285,53 @@ __device__ __forceinline__ float xfold(float (&v)[N]) {
 }
 
 // Fixed-order merge of the warps' (m, l, o) for G heads; writes the
-// normalised partial row and its log2-sum-exp2. mg holds [W][G*D] outputs,
-// then [W][G] maxima, then [W][G] sums.
+// normalised partial row and its log2-sum-exp2. mg holds [W][G] output rows
+// of gqa_merge_row(D) floats, then [W][G] maxima, [W][G] sums and room for
+// [W][G] weights. Thread h < G first folds head h's statistics in warp order
+// into one weight per warp, w_wh = 2^(m_wh - M_h) / sum_w' 2^(m_w'h - M_h) l_w'h,
+// and the head's lse; then every output element is sum_w w_wh o_wh[d] in
+// warp order, four columns per thread.
 template <int D>
 __device__ __forceinline__ void merge_warps(const Stage1Args& a, const pkvd_work_item& it, int G,
-                                            int hq0, const float* mg) {
+                                            int hq0, float* mg) {
   constexpr int W = gqa_warps(D);
-  const float* mm = mg + W * G * D;
+  constexpr int RS = gqa_merge_row(D);
+  const float* mm = mg + W * G * RS;
   const float* ml = mm + W * G;
-  for (int idx = threadIdx.x; idx < G * D; idx += W * 32) {
-    const int h = idx / D, d = idx % D;
+  float* wt = mg + W * G * RS + 2 * W * G;
+  const int64_t row0 = static_cast<int64_t>(it.partial_row) * a.heads + hq0;
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * G + h]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
+    float e[W];
+    float den = 0.f;
 #pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float e = exp2f(mm[w * G + h] - M);
-        den += e * ml[w * G + h];
-        num += e * mg[w * G * D + h * D + d];
-      }
+    for (int w = 0; w < W; ++w) {
+      e[w] = M == -INFINITY ? 0.f : exp2f(mm[w * G + h] - M);
+      den += e[w] * ml[w * G + h];
     }
-    const int64_t row = static_cast<int64_t>(it.partial_row) * a.heads + hq0 + h;
-    a.o_part[row * a.dv + d] = (M == -INFINITY) ? 0.f : num / den;
-    if (d == 0) a.lse_part[row] = (M == -INFINITY) ? -INFINITY : M + log2f(den);
+    const float inv = M == -INFINITY ? 0.f : 1.f / den;
+#pragma unroll
+    for (int w = 0; w < W; ++w) wt[w * G + h] = e[w] * inv;
+    a.lse_part[(hq0 + h) * a.lse_stride + it.partial_row] =
+        M == -INFINITY ? -INFINITY : M + log2f(den);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * (D / 4); idx += W * 32) {
+    const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float c = wt[w * G + h];
+      const float4 o = *reinterpret_cast<const float4*>(mg + (w * G + h) * RS + d);
+      acc.x = fmaf(c, o.x, acc.x);
+      acc.y = fmaf(c, o.y, acc.y);
+      acc.z = fmaf(c, o.z, acc.z);
+      acc.w = fmaf(c, o.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(a.o_part + (row0 + h) * a.dv + d) = acc;
   }
 }
 
@@ -312,12 +352,17 @@ __global__ void __launch_bounds__(gqa_threads(D), 1)
                 "merge area must fit in the stage area");
 
   extern __shared__ uint8_t smem_raw[];
+  if (TILES && threadIdx.x == 0) {
+    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.v);
+  }
   const pkvd_work_item it = a.items[blockIdx.x];
   pdl_launch_dependents();
   const GqaSmem<D, G, TILES> sm(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WarpRows<D, TILES> wr(a, it, warp, lane);
   init_stage_barriers<D>(sm.bars);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* pb = sm.pbuf + warp * (BLK * GP + GP);
   const int kvh = it.unit;
   const int f = lane >> SHIFT;            // (key in pass, head) this lane ends with
@@ -347,7 +392,7 @@ __global__ void __launch_bounds__(gqa_threads(D), 1)
     for (int c = 0; c < CH; ++c) acc[h][c] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;
 
-  const bool ok = gqa_warp_loop<D, TILES>(a, maps, it, sm.stages, sm.bars, warp, lane, load_q,
+  const bool ok = gqa_warp_loop<D, TILES>(a, maps, it, wr, sm.stages, sm.bars, warp, lane, load_q,
                                           [&](int nv, const uint8_t* ks) {
     const uint8_t* vs = ks + TB;
     float sc[4];
@@ -427,15 +472,18 @@ __global__ void __launch_bounds__(gqa_threads(D), 1)
     return;
   }
   // All stages are consumed: reuse them for the cross-warp merge.
+  constexpr int RS = gqa_merge_row(D);
   float* mg = reinterpret_cast<float*>(sm.stages);
-  float* mo = mg + warp * G * D;
+  float* mo = mg + warp * G * RS;
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int c = 0; c < CH; ++c) mo[h * D + lane * CH + c] = acc[h][c];
+    for (int c = 0; c < CH; c += 4)
+      *reinterpret_cast<float4*>(mo + h * RS + lane * CH + c) =
+          make_float4(acc[h][c], acc[h][c + 1], acc[h][c + 2], acc[h][c + 3]);
   if (primary && fk == 0) {
-    mg[W * G * D + warp * G + fh] = m_run;
-    mg[W * G * D + W * G + warp * G + fh] = l_run;
+    mg[W * G * RS + warp * G + fh] = m_run;
+    mg[W * G * RS + W * G + warp * G + fh] = l_run;
   }
   __syncthreads();
   merge_warps<D>(a, it, G, kvh * G, mg);
@@ -454,6 +502,10 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
                 "merge area must fit in the stage area");
 
   extern __shared__ uint8_t smem_raw[];
+  if (TILES && threadIdx.x == 0) {
+    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.v);
+  }
   const pkvd_work_item it = a.items[blockIdx.x];
   pdl_launch_dependents();
   const GqaSmem<D, GMAX, TILES> sm(smem_raw);
@@ -463,6 +515,7 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
   const int G = a.heads / a.kv_heads;
   const int kvh = it.unit;
 
+  WarpRows<D, TILES> wr(a, it, warp, lane);
   init_stage_barriers<D>(sm.bars);
 
   // The group's query rows [GMAX][D] in padded rows (zero past G): the
@@ -505,7 +558,7 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
   const int vr = ((lane >> 4) & 1) * 8 + (lane & 7), vhi = (lane >> 3) & 1;
   const uint32_t qaddr = smem_addr(sm.qtile + (lane & 7) * gqa_row_pitch(D) + (lane >> 3) * 16);
 
-  const bool ok = gqa_warp_loop<D, TILES>(a, maps, it, sm.stages, sm.bars, warp, lane, load_q,
+  const bool ok = gqa_warp_loop<D, TILES>(a, maps, it, wr, sm.stages, sm.bars, warp, lane, load_q,
                                           [&](int nv, uint8_t* ks_) {
     uint8_t* vs = ks_ + TB;
     if (nv < BLK) {
@@ -622,20 +675,21 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
     if (threadIdx.x == 0) atomicOr(a.status, kStatusTimeout);
     return;
   }
+  constexpr int RS = gqa_merge_row(D);
   float* mg = reinterpret_cast<float*>(sm.stages);
-  float* mo = mg + warp * G * D;
+  float* mo = mg + warp * G * RS;
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h0 = nt * 8 + 2 * t, d0 = mt * 16 + g;
       if (h0 < G) {
-        mo[h0 * D + d0] = o[mt][nt][0];
-        mo[h0 * D + d0 + 8] = o[mt][nt][2];
+        mo[h0 * RS + d0] = o[mt][nt][0];
+        mo[h0 * RS + d0 + 8] = o[mt][nt][2];
       }
       if (h0 + 1 < G) {
-        mo[(h0 + 1) * D + d0] = o[mt][nt][1];
-        mo[(h0 + 1) * D + d0 + 8] = o[mt][nt][3];
+        mo[(h0 + 1) * RS + d0] = o[mt][nt][1];
+        mo[(h0 + 1) * RS + d0 + 8] = o[mt][nt][3];
       }
     }
   if (g == 0) {
@@ -645,8 +699,8 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
       for (int e = 0; e < 2; ++e) {
         const int h = nt * 8 + 2 * t + e;
         if (h < G) {
-          mg[W * G * D + warp * G + h] = m_run[nt][e];
-          mg[W * G * D + W * G + warp * G + h] = l_run[nt][e];
+          mg[W * G * RS + warp * G + h] = m_run[nt][e];
+          mg[W * G * RS + W * G + warp * G + h] = l_run[nt][e];
         }
       }
   }

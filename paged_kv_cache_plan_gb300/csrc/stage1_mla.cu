@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
       *reinterpret_cast<float2*>(orow + q * 8) =
           make_float2(o[q][2 * r] * inv, o[q][2 * r + 1] * inv);
     if (warp == 0 && t == 0)
-      a.lse_part[row0 + h] = empty ? -INFINITY : m_run[r] + log2f(l_run[r]);
+      a.lse_part[(it.unit * HB + h) * a.lse_stride + it.partial_row] =
+          empty ? -INFINITY : m_run[r] + log2f(l_run[r]);
   }
 }
 

@@ -174,6 +174,14 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
                      (r - m * a.heads)
                : -1;
   };
+  // Partial-lse index of query row r (head-major lse array; -1: unused).
+  auto lse_idx = [&](int r) -> int64_t {
+    if (!it.grouped) return static_cast<int64_t>(it.unit * R + r) * a.lse_stride + it.partial_row;
+    const int m = r / a.heads;
+    return m < it.unit ? static_cast<int64_t>(r - m * a.heads) * a.lse_stride +
+                             a.split_base[it.request + m] + it.split
+                       : -1;
+  };
   // Q tile: the 64 query rows, K-major (unused rows zero).
   {
     for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
@@ -489,8 +497,8 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
             const int col = 32 * h + 2 * cl + e;
             const float l = ((red[col] + red[64 + col]) + red[128 + col]) + red[192 + col];
             alpha_s[col] = nblk > 0 ? 1.f / l : 0.f;
-            const int64_t orow = out_row(col);
-            if (orow >= 0) a.lse_part[orow] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
+            const int64_t li = lse_idx(col);
+            if (li >= 0) a.lse_part[li] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
           }
         }
         named_sync(1, SMX);

@@ -9,11 +9,15 @@
 // Grid: (B * Hq, tiles). With tiles > 1 each block owns a disjoint slice of
 // the Dv output columns and re-derives M and sum_s w_s on its own, so the
 // slices never communicate -- the head-dim-tiled stage-2 reduce of the
-// aiter pull 4758 page (Technical Details 3). M and the weight sum are
-// always computed by warp 0 in the same lane-strided order, and the weighted
-// sums run over a fixed split-residue layout, so every tiling gives
-// identical bits. The merge waits on stage 1 with griddepcontrol.wait,
-// so it can be launched early (programmatic dependent launch).
+// aiter pull 4758 page (Technical Details 3). The merge waits on stage 1
+// with griddepcontrol.wait, so it can be launched early (programmatic
+// dependent launch).
+//
+// Bit-identical results for every tiling: every warp computes M and the
+// weight sum itself, from the split lse values in the same lane-strided
+// order with a xor butterfly (so all lanes and warps hold the same bits),
+// and each float4 column is summed in a layout fixed by the split index
+// alone (below), whichever block or thread owns the column.
 #include "device.cuh"
 #include "kernels.h"
 
@@ -21,22 +25,42 @@ namespace pkvd {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kSplitGroups = 16;    // splits s = g, g + 16, g + 32, ... per group
-constexpr int kColThreads = 16;     // float4 columns per pass
+constexpr int kSplitGroups = 32;    // splits s = g, g + 32, g + 64, ... per group
+constexpr int kColThreads = 8;      // float4 columns per pass
+constexpr int kWarps = kMergeThreads / 32;
 static_assert(kMergeThreads == kSplitGroups * kColThreads, "merge block shape");
+static_assert(stage2_smem_bytes(4) == kWarps * 16, "one float4 per warp and column");
 
-// Block layout: thread (g, c) = (tid / 16, tid % 16) sums, for each of its
-// float4 columns c, c + 16, ..., the weighted partials of splits s = g mod 16
-// in increasing s; the 16 group sums are then added in group order. The
-// order of every addition depends only on s and the column, never on the
-// tiling, so all tilings give identical bits.
-// kPre: partials per thread loaded before the weights are known. Deep (8)
-// when the merge grid is small and latency-bound; shallow (2) when it is
-// large, where the extra registers would cost occupancy.
-template <int kPre>
-__global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_constant__ Stage2Args a) {
-  extern __shared__ float4 dyn[];   // [16][C4] group sums, then [S] weights
-  __shared__ float stats[2];        // M, sum of weights
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& x) {
+  acc.x = fmaf(w, x.x, acc.x);
+  acc.y = fmaf(w, x.y, acc.y);
+  acc.z = fmaf(w, x.z, acc.z);
+  acc.w = fmaf(w, x.w, acc.w);
+}
+
+__device__ __forceinline__ void add_xor4(float4& v, int m) {
+  v.x += __shfl_xor_sync(kFull, v.x, m);
+  v.y += __shfl_xor_sync(kFull, v.y, m);
+  v.z += __shfl_xor_sync(kFull, v.z, m);
+  v.w += __shfl_xor_sync(kFull, v.w, m);
+}
+
+// Block layout: thread (g, c) = (tid / 8, tid % 8) sums, for each of its
+// float4 columns c, c + 8, ..., the weighted partials of splits s = g mod 32
+// in increasing s. The four groups of a warp are added by a xor butterfly
+// over lane bits 3-4, the eight warps' sums in warp order. Each lane holds
+// kLseRegs lse values (lane-strided) and the weights of its first kLseRegs
+// own splits in registers; further splits are read as they come. kPre:
+// partials per thread (of its first column) loaded together with the lse
+// values, before the weights are known -- all of a thread's splits when
+// S <= 32 kPre -- and the number of partial loads in flight per thread after
+// that. Deep (8, 8) when the merge grid is small and latency-bound; shallow
+// (2, 2) when it is large, where registers would cost occupancy.
+template <int kPre, int kLseRegs>
+__global__ void __launch_bounds__(kMergeThreads, kPre > 2 ? 2 : 5)
+    merge_splits(const __grid_constant__ Stage2Args a) {
+  static_assert(kLseRegs % kPre == 0, "prefetch depth divides the register window");
+  extern __shared__ float4 wsum4[];   // [kWarps][C4] warp sums
 
   const int bh = blockIdx.x;
   const int b = bh / a.heads;
@@ -44,21 +68,24 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
   const int dt = a.dv / a.tiles;
   const int C4 = dt / 4;
   const int d0 = blockIdx.y * dt;
-  float4* gsum = dyn;
-  float* w_s = reinterpret_cast<float*>(dyn + kSplitGroups * C4);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = threadIdx.x / kColThreads;
+  const int ct = threadIdx.x % kColThreads;
+
+  // The split table is written at plan time, not by stage 1: read it before
+  // the wait, while stage 1 finishes.
+  const int r0 = a.split_base[b];
+  const int S = a.split_base[b + 1] - r0;
 
   pdl_wait_prerequisites();
 
-  const int r0 = a.split_base[b];
-  const int S = a.split_base[b + 1] - r0;
-  const int grp = threadIdx.x / kColThreads;
-  const int ct = threadIdx.x % kColThreads;
   const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
   const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
+  const float* lp = a.lse_part + h * a.lse_stride + r0;   // this head's splits
 
-  // The first kPre partials of this thread's first column are loaded right
-  // away, in flight together with the split log-sum-exps: the weights need
-  // the lse values, the loads do not.
+  // One round trip: the first kPre partials of this thread's first column,
+  // and the lse values (lane-strided, for M and the weight sum; and those of
+  // this thread's own splits grp + 32 i).
   float4 pre[kPre];
 #pragma unroll
   for (int u = 0; u < kPre; ++u) {
@@ -66,67 +93,75 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
     pre[u] = ct < C4 && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + ct)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int s = threadIdx.x; s < S; s += kMergeThreads)
-    w_s[s] = a.lse_part[static_cast<int64_t>(r0 + s) * a.heads + h];
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float m = -INFINITY;
-    for (int s = lane; s < S; s += 32) m = fmaxf(m, w_s[s]);
+  float lv[kLseRegs], lo[kLseRegs];
 #pragma unroll
-    for (int x = 16; x >= 1; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
-    float ws = 0.f;
-    for (int s = lane; s < S; s += 32) {
-      const float w = (m == -INFINITY) ? 0.f : exp2f(w_s[s] - m);
-      w_s[s] = w;
-      ws += w;
-    }
-#pragma unroll
-    for (int x = 16; x >= 1; x >>= 1) ws += __shfl_xor_sync(kFull, ws, x);
-    if (lane == 0) {
-      stats[0] = m;
-      stats[1] = ws;
-    }
+  for (int i = 0; i < kLseRegs; ++i) {
+    const int s = lane + 32 * i, so = grp + kSplitGroups * i;
+    lv[i] = s < S ? __ldg(lp + s) : -INFINITY;
+    lo[i] = so < S ? __ldg(lp + so) : -INFINITY;
   }
-  __syncthreads();
-  const float M = stats[0];
-  const float wsum = stats[1];
-  const bool empty = (M == -INFINITY);
-  const float inv = empty ? 0.f : 1.f / wsum;
 
-  auto fma4 = [](float4& acc, float w, const float4& x) {
-    acc.x = fmaf(w, x.x, acc.x);
-    acc.y = fmaf(w, x.y, acc.y);
-    acc.z = fmaf(w, x.z, acc.z);
-    acc.w = fmaf(w, x.w, acc.w);
-  };
-  for (int c = ct; c < C4; c += kColThreads) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kLseRegs; ++i) m = fmaxf(m, lv[i]);
+  for (int s = lane + 32 * kLseRegs; s < S; s += 32)
+    m = fmaxf(m, __ldg(lp + s));
+#pragma unroll
+  for (int x = 16; x >= 1; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
+  const bool empty = (m == -INFINITY);
+  float ws = 0.f;
+  if (!empty) {
+#pragma unroll
+    for (int i = 0; i < kLseRegs; ++i) ws += exp2f(lv[i] - m);
+    for (int s = lane + 32 * kLseRegs; s < S; s += 32)
+      ws += exp2f(__ldg(lp + s) - m);
+  }
+#pragma unroll
+  for (int x = 16; x >= 1; x >>= 1) ws += __shfl_xor_sync(kFull, ws, x);
+  const float inv = empty ? 0.f : 1.f / ws;
+  auto weight = [&](float l) { return empty ? 0.f : exp2f(l - m); };
+  float wo[kLseRegs];
+#pragma unroll
+  for (int i = 0; i < kLseRegs; ++i) wo[i] = weight(lo[i]);
+
+  for (int c0 = 0; c0 < C4; c0 += kColThreads) {
+    const int c = c0 + ct;
+    const bool valid = c < C4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = grp;
-    if (c == ct) {
+    // own splits below 32 kLseRegs, kPre loads in flight at a time (the
+    // terms past S are zero, so stopping there changes no bits)
 #pragma unroll
-      for (int u = 0; u < kPre; ++u, s += kSplitGroups)
-        if (s < S) fma4(acc, w_s[s], pre[u]);
+    for (int i0 = 0; i0 < kLseRegs; i0 += kPre) {
+      if (grp + kSplitGroups * i0 >= S) break;
+      float4 x[kPre];
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const int s = grp + kSplitGroups * (i0 + j);
+        if (i0 == 0 && c0 == 0)
+          x[j] = pre[j];
+        else
+          x[j] = valid && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) fma4(acc, wo[i0 + j], x[j]);
     }
-    for (; s + 3 * kSplitGroups < S; s += 4 * kSplitGroups) {
-      float4 x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        x[u] = __ldg(reinterpret_cast<const float4*>(base + (s + u * kSplitGroups) * stride) + c);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) fma4(acc, w_s[s + u * kSplitGroups], x[u]);
+    for (int s = grp + kSplitGroups * kLseRegs; s < S; s += kSplitGroups) {
+      const float l = __ldg(lp + s);
+      fma4(acc, weight(l), valid ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f));
     }
-    for (; s < S; s += kSplitGroups)
-      fma4(acc, w_s[s], __ldg(reinterpret_cast<const float4*>(base + s * stride) + c));
-    gsum[grp * C4 + c] = acc;
+    add_xor4(acc, 8);
+    add_xor4(acc, 16);
+    if (lane < kColThreads && valid) wsum4[warp * C4 + c] = acc;
   }
   __syncthreads();
   float* out = a.out + static_cast<int64_t>(bh) * a.dv + d0;
   for (int c = threadIdx.x; c < C4; c += kMergeThreads) {
-    float4 t = gsum[c];
+    float4 t = wsum4[c];
 #pragma unroll
-    for (int g = 1; g < kSplitGroups; ++g) {
-      const float4 x = gsum[g * C4 + c];
+    for (int w = 1; w < kWarps; ++w) {
+      const float4 x = wsum4[w * C4 + c];
       t.x += x.x;
       t.y += x.y;
       t.z += x.z;
@@ -135,17 +170,99 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits(const __grid_const
     reinterpret_cast<float4*>(out)[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
   }
   if (blockIdx.y == 0 && threadIdx.x == 0)
-    a.lse[bh] = empty ? -INFINITY : (M + log2f(wsum)) * 0.69314718055994530942f;
+    a.lse[bh] = empty ? -INFINITY : (m + log2f(ws)) * 0.69314718055994530942f;
+}
+
+// Few splits (S <= kMergeColMaxSplits for every request): one thread per
+// float4 column, all S partials in flight at once. The column sum is formed
+// in exactly the order merge_splits uses for such S -- product w_s o_s per
+// split (split s alone in its residue group), xor butterfly over groups
+// (0+1)+(2+3) and (4+5)+(6+7) within a warp, then warp 0's sum plus warp
+// 1's -- and M and the weight sum by the same warp code, so both kernels
+// give identical bits.
+__global__ void __launch_bounds__(128) merge_cols(const __grid_constant__ Stage2Args a) {
+  constexpr int NS = kMergeColMaxSplits;
+  static_assert(NS == 8, "the fixed summation tree below covers eight splits");
+  const int bh = blockIdx.x;
+  const int b = bh / a.heads;
+  const int h = bh - b * a.heads;
+  const int dt = a.dv / a.tiles;
+  const int C4 = dt / 4;
+  const int d0 = blockIdx.y * dt;
+  const int lane = threadIdx.x & 31;
+
+  // The split table is written at plan time, not by stage 1: read it before
+  // the wait, while stage 1 finishes.
+  const int r0 = a.split_base[b];
+  const int S = a.split_base[b + 1] - r0;
+
+  pdl_wait_prerequisites();
+
+  const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
+  const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
+  const float* lp = a.lse_part + h * a.lse_stride + r0;   // this head's splits
+
+  float ls[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) ls[s] = s < S ? __ldg(lp + s) : -INFINITY;
+  // M and the weight sum as merge_splits' warps form them (lane s holds split s)
+  float lv = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < NS; ++s)
+    if (lane == s) lv = ls[s];
+  float m = lv;
+#pragma unroll
+  for (int x = 16; x >= 1; x >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, x));
+  const bool empty = (m == -INFINITY);
+  float ws = empty ? 0.f : exp2f(lv - m);
+#pragma unroll
+  for (int x = 16; x >= 1; x >>= 1) ws += __shfl_xor_sync(kFull, ws, x);
+  const float inv = empty ? 0.f : 1.f / ws;
+  float w[NS];
+#pragma unroll
+  for (int s = 0; s < NS; ++s) w[s] = empty ? 0.f : exp2f(ls[s] - m);
+
+  float* out = a.out + static_cast<int64_t>(bh) * a.dv + d0;
+  for (int c = threadIdx.x; c < C4; c += blockDim.x) {
+    float4 t[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      t[s] = s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+      fma4(p, w[s], t[s]);
+      t[s] = p;
+    }
+    auto add = [](const float4& x, const float4& y) {
+      return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+    };
+    const float4 w0 = add(add(t[0], t[1]), add(t[2], t[3]));
+    const float4 w1 = add(add(t[4], t[5]), add(t[6], t[7]));
+    const float4 r = add(w0, w1);
+    reinterpret_cast<float4*>(out)[c] = make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
+  }
+  if (blockIdx.y == 0 && threadIdx.x == 0)
+    a.lse[bh] = empty ? -INFINITY : (m + log2f(ws)) * 0.69314718055994530942f;
 }
 
 }  // namespace
 
-bool stage2_kernel(bool deep_prefetch, KernelEntry* e) {
-  e->func = deep_prefetch ? reinterpret_cast<const void*>(&merge_splits<8>)
-                          : reinterpret_cast<const void*>(&merge_splits<2>);
-  e->threads = kMergeThreads;
-  e->smem = 0;      // per plan: stage2_smem_bytes(Dv / tiles, max splits)
-  return true;
+bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, KernelEntry* e) {
+  const int tiles = info.stage2_tiles > 0 ? info.stage2_tiles : 1;
+  if (info.max_splits <= kMergeColMaxSplits) {
+    e->func = reinterpret_cast<const void*>(&merge_cols);
+    e->threads = merge_col_threads(dv / tiles);
+    e->smem = 0;
+  } else {
+    const bool deep = static_cast<int64_t>(batch) * heads * tiles <= 2LL * info.num_sms;
+    e->func = deep ? reinterpret_cast<const void*>(&merge_splits<8, 8>)
+                   : reinterpret_cast<const void*>(&merge_splits<2, 2>);
+    e->threads = kMergeThreads;
+    e->smem = stage2_smem_bytes(dv / tiles);
+  }
+  return e->threads == info.stage2_threads;
 }
 
 }  // namespace pkvd

@@ -106,10 +106,8 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     return PKVD_ENOMEM;
   }
   if (rc != PKVD_OK) return rc;
-  pkvd::stage2_kernel(pkvd::merge_prefers_deep(static_cast<int64_t>(L.desc.batch) * L.desc.heads *
-                                                   L.info.stage2_tiles,
-                                               L.desc.num_sms),
-                      &s2);
+  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.heads, L.desc.head_dim_v, &s2))
+    return PKVD_EUNSUPPORTED;   // the plan's merge shape and the kernel table disagree
   const bool any_work = L.info.num_items > 0;
   if (any_work && (!q || !k_pages || !v_pages || !page_table)) return PKVD_EINVAL;
   if (any_work && (!aligned16_static(q) || !aligned16_static(k_pages) ||
@@ -157,6 +155,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     a.items = d_items;
     a.o_part = d_opart;
     a.lse_part = d_lpart;
+    a.lse_stride = L.info.num_partial_rows;
     a.status = d_status;
     a.pt_stride = L.desc.max_pages_per_seq;
     a.k_pitch = L.desc.k_row_pitch;
@@ -181,6 +180,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   pkvd::Stage2Args m{};
   m.o_part = d_opart;
   m.lse_part = d_lpart;
+  m.lse_stride = L.info.num_partial_rows;
   m.split_base = d_split;
   m.out = out;
   m.lse = lse;
@@ -192,8 +192,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   cfg.gridDim = dim3(static_cast<unsigned>(L.desc.batch * L.desc.heads),
                      static_cast<unsigned>(m.tiles));
   cfg.blockDim = dim3(static_cast<unsigned>(L.info.stage2_threads));
-  cfg.dynamicSmemBytes = static_cast<size_t>(
-      pkvd::stage2_smem_bytes(L.desc.head_dim_v / L.info.stage2_tiles, L.info.max_splits));
+  cfg.dynamicSmemBytes = static_cast<size_t>(s2.smem);
   if (cudaFuncSetAttribute(s2.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(cfg.dynamicSmemBytes)) != cudaSuccess)
     return PKVD_ECUDA;

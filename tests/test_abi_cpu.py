@@ -258,3 +258,33 @@ def test_shared_prefix_needs_mla(L):
         decode_plan_prefix_compute(make_desc(2, 8, 2, 128, 16, num_sms=152, ctas_per_sm=1),
                                    [32, 32], [0, 0], [16, 16])
     assert e.value.code == _lib.PKVD_EUNSUPPORTED
+
+
+def _merge_threads(max_splits, dv_slice):
+    # one thread per float4 column (blocks of 32..128) for at most 8 splits,
+    # else the 256-thread split-parallel merge
+    if max_splits <= 8:
+        return min(128, max(32, -(-(dv_slice // 4) // 32) * 32))
+    return 256
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 16, 2, 256, 16, [65536], {}),                 # many splits
+    (1, 4, 1, 128, 16, [512], {"splits": 4}),         # few splits, sliced Dv
+    (64, 128, 1, 576, 1, [16384] * 64, {}),           # few splits, untiled 512
+    (10, 32, 8, 128, 16, [256, 512, 8192, 65536] + [1024] * 6, {}),
+])
+def test_merge_block_shape(L, shape):
+    B, H, Hkv, D, ps, seq, kw = shape
+    info, _ = _plan(B, H, Hkv, D, ps, seq=seq, **kw)
+    dv = 512 if D == 576 else D
+    assert info["stage2_threads"] == _merge_threads(info["max_splits"], dv // info["stage2_tiles"])
+
+
+def test_merge_block_shape_follows_prefix_splits(L):
+    # the prefix splits raise the per-request split count after the private
+    # tokens were planned; the merge shape must follow the final count
+    for B, seq, plen in ((8, [68000] * 8, [63240] * 8), (2, [3000, 3000], [2900, 2900])):
+        info, _, _ = _prefix_plan(B, 16, seq, [0] * B, plen)
+        assert info["stage2_threads"] == _merge_threads(info["max_splits"],
+                                                        512 // info["stage2_tiles"])
