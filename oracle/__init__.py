@@ -39,6 +39,7 @@ MUTATIONS = {
     "pages_reversed": 8,
     "merge_no_norm": 9,
     "drop_last_key": 10,
+    "no_causal": 11,
 }
 
 
@@ -56,6 +57,7 @@ class Problem(ctypes.Structure):
         ("k_row_pitch", ctypes.c_int64),
         ("v_row_pitch", ctypes.c_int64),
         ("scale", ctypes.c_double),
+        ("q_len", ctypes.c_int32),
     ]
 
 
@@ -122,12 +124,12 @@ def _i32(a):
 
 
 def problem(*, batch, heads, kv_heads, head_dim, head_dim_v, page_size, dtype,
-            max_pages, k_row_pitch, v_row_pitch, scale, mutation=0) -> Problem:
+            max_pages, k_row_pitch, v_row_pitch, scale, mutation=0, q_len=1) -> Problem:
     return Problem(int(batch), int(heads), int(kv_heads), int(head_dim),
                    int(head_dim_v), int(page_size),
                    FP16 if dtype in ("fp16", FP16) else BF16, int(mutation),
                    int(max_pages), int(k_row_pitch), int(v_row_pitch),
-                   float(scale))
+                   float(scale), int(q_len))
 
 
 def _check(rc, what):
@@ -137,10 +139,11 @@ def _check(rc, what):
 
 def decode(P: Problem, q, k_pages, v_pages, page_table, seq_lens, *,
            pairs=None, threads: int = 0):
-    """fp64 out and lse. With ``pairs`` ([n, 2] of (b, h)) only those heads
-    are computed and the results come back as out [n, Dv], lse [n]; otherwise
-    out [B, Hq, Dv], lse [B, Hq]. ``threads`` > 0 spreads the full decode
-    over that many host threads (same arithmetic per head)."""
+    """fp64 out and lse. With ``pairs`` ([n, 2] of (b, v), v = token * Hq +
+    head) only those are computed and the results come back as out [n, Dv],
+    lse [n]; otherwise out [B, q_len * Hq, Dv], lse [B, q_len * Hq] (q_len =
+    1: [B, Hq, ...]). ``threads`` > 0 spreads the full decode over that many
+    host threads (same arithmetic per head)."""
     L = lib()
     pt, sl = _i32(page_table), _i32(seq_lens)
     if pairs is not None:
@@ -152,8 +155,9 @@ def decode(P: Problem, q, k_pages, v_pages, page_table, seq_lens, *,
                                   _ptr(v_pages), _ptr(pt), _ptr(sl), _ptr(pr),
                                   n, _ptr(out), _ptr(lse)), "decode_pairs")
         return out, lse
-    out = np.zeros((P.batch, P.heads, P.head_dim_v), dtype=np.float64)
-    lse = np.zeros((P.batch, P.heads), dtype=np.float64)
+    vh = max(P.q_len, 1) * P.heads
+    out = np.zeros((P.batch, vh, P.head_dim_v), dtype=np.float64)
+    lse = np.zeros((P.batch, vh), dtype=np.float64)
     if threads and threads > 0:
         _check(L.orc_decode_threads(ctypes.byref(P), _ptr(q), _ptr(k_pages),
                                     _ptr(v_pages), _ptr(pt), _ptr(sl),
@@ -167,7 +171,8 @@ def decode(P: Problem, q, k_pages, v_pages, page_table, seq_lens, *,
 
 
 def scores(P: Problem, q, k_pages, page_table, seq_lens, b: int, h: int):
-    """Scaled fp64 scores of (b, h) in logical token order."""
+    """Scaled fp64 scores of (b, v) (v = token * Hq + head) for all of the
+    request's tokens in logical order (no causal cut)."""
     L = lib()
     pt, sl = _i32(page_table), _i32(seq_lens)
     n = int(np.asarray(sl)[b]) if not hasattr(sl, "data_ptr") else int(sl[b])
@@ -178,7 +183,8 @@ def scores(P: Problem, q, k_pages, page_table, seq_lens, b: int, h: int):
 
 
 def partial(P: Problem, q, k_pages, v_pages, page_table, seq_lens, b, h, t0, t1):
-    """Normalised partial output and lse of (b, h) over tokens [t0, t1)."""
+    """Normalised partial output and lse of (b, v) over the tokens of
+    [t0, t1) that query token v // Hq may see."""
     L = lib()
     pt, sl = _i32(page_table), _i32(seq_lens)
     o = np.zeros((P.head_dim_v,), dtype=np.float64)

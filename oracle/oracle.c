@@ -22,6 +22,15 @@
  * An empty request (L_b = 0) gives out = 0 and lse = -inf. Everything is
  * double precision; bf16 and fp16 inputs convert to double exactly.
  *
+ * Several query tokens per request (q_len >= 1: draft tokens checked in one
+ * step, as in the rocm-libraries page's served models that decode with
+ * multi-token-prediction drafts). The request's last q_len tokens are its
+ * queries, already in the cache: query token j (0-based) sits at position
+ * L_b - q_len + j and attends to the keys at or before its own position,
+ * t = 0 .. L_b - q_len + j. q is [B, q_len, Hq, D] and out / lse follow the
+ * same (request, token, head) order; "virtual head" v = j * Hq + h indexes
+ * the (token, head) pairs of one request. q_len = 1 is the plain decode.
+ *
  * The split partial and the merge follow the aiter pull 4758 page
  * ("[Gluon][MLA] Deeper async-copy pipeline in the bh16 stage-1 decode
  * loop"), Motivation and Technical Details 3: each split of a request's
@@ -55,6 +64,7 @@
 #define MUT_PAGES_REVERSED 8  /* page_table walked from the far end         */
 #define MUT_MERGE_NO_NORM 9   /* merge divides by the split count           */
 #define MUT_DROP_LAST_KEY 10  /* the last token of a request is skipped      */
+#define MUT_NO_CAUSAL 11      /* every query token sees all L_b keys         */
 
 typedef struct {
   int32_t batch;
@@ -69,7 +79,10 @@ typedef struct {
   int64_t k_row_pitch; /* elements between consecutive K rows             */
   int64_t v_row_pitch; /* elements between consecutive V rows             */
   double scale;        /* multiplies q.k                                   */
+  int32_t q_len;       /* query tokens per request; 0 counts as 1          */
 } orc_problem;
+
+static int q_len_of(const orc_problem *P) { return P->q_len > 0 ? P->q_len : 1; }
 
 /* bf16 is the top half of an IEEE binary32: widen and reinterpret. */
 static double bf16_to_double(uint16_t bits) {
@@ -125,13 +138,14 @@ static int kv_head_of(const orc_problem *P, int h) {
   return h / g;
 }
 
-/* Scaled scores s_t for t in [t0, t1) of (b, h) into s[0 .. t1-t0). */
+/* Scaled scores s_t for t in [t0, t1) of (b, v) into s[0 .. t1-t0), where
+ * v = j * heads + h is query token j's head h. */
 static void scores(const orc_problem *P, const uint16_t *q, const uint16_t *k,
                    const int32_t *page_table, const int32_t *seq_lens, int b,
-                   int h, int64_t t0, int64_t t1, double *s) {
+                   int v, int64_t t0, int64_t t1, double *s) {
   int D = P->head_dim;
-  int kv = kv_head_of(P, h);
-  const uint16_t *qrow = q + ((int64_t)b * P->heads + h) * D;
+  int kv = kv_head_of(P, v % P->heads);
+  const uint16_t *qrow = q + ((int64_t)b * q_len_of(P) * P->heads + v) * D;
   double scale = P->mutation == MUT_NO_SCALE ? 1.0 : P->scale;
   for (int64_t t = t0; t < t1; ++t) {
     const uint16_t *krow =
@@ -143,15 +157,20 @@ static void scores(const orc_problem *P, const uint16_t *q, const uint16_t *k,
   }
 }
 
-/* Softmax-weighted V over tokens [t0, t1) of (b, h): out[0:Dv] and lse.
- * An empty range gives out = 0, lse = -inf. Returns 0, or -1 on OOM. */
+/* Softmax-weighted V over the tokens of [t0, t1) that (b, vh) may see:
+ * out[0:Dv] and lse. vh = j * heads + h; query token j sees the tokens
+ * t <= L_b - q_len + j. An empty range gives out = 0, lse = -inf. Returns 0,
+ * or -1 on OOM. */
 static int attend_range(const orc_problem *P, const uint16_t *q,
                         const uint16_t *k, const uint16_t *v,
                         const int32_t *page_table, const int32_t *seq_lens,
-                        int b, int h, int64_t t0, int64_t t1, double *out,
+                        int b, int vh, int64_t t0, int64_t t1, double *out,
                         double *lse) {
   int Dv = P->head_dim_v;
   for (int d = 0; d < Dv; ++d) out[d] = 0.0;
+  int64_t visible = (int64_t)seq_lens[b] - q_len_of(P) + vh / P->heads + 1;
+  if (P->mutation == MUT_NO_CAUSAL) visible = seq_lens[b];
+  if (t1 > visible) t1 = visible;
   if (P->mutation == MUT_DROP_LAST_KEY && t1 == seq_lens[b] && t1 > t0) --t1;
   int64_t n = t1 - t0;
   if (n <= 0) {
@@ -160,7 +179,7 @@ static int attend_range(const orc_problem *P, const uint16_t *q,
   }
   double *s = (double *)malloc((size_t)n * sizeof(double));
   if (!s) return -1;
-  scores(P, q, k, page_table, seq_lens, b, h, t0, t1, s);
+  scores(P, q, k, page_table, seq_lens, b, vh, t0, t1, s);
 
   double m = -INFINITY;
   for (int64_t i = 0; i < n; ++i)
@@ -169,7 +188,7 @@ static int attend_range(const orc_problem *P, const uint16_t *q,
 
   const uint16_t *vpool = P->mutation == MUT_V_FROM_K ? k : v;
   int64_t vpitch = P->mutation == MUT_V_FROM_K ? P->k_row_pitch : P->v_row_pitch;
-  int kv = kv_head_of(P, h);
+  int kv = kv_head_of(P, vh % P->heads);
   double z = 0.0;
   for (int64_t i = 0; i < n; ++i) {
     double w = exp(s[i] - m);
@@ -191,10 +210,12 @@ static int check_problem(const orc_problem *P) {
     return -2;
   if (P->heads % P->kv_heads) return -2;
   if (P->dtype != ORC_BF16 && P->dtype != ORC_FP16) return -2;
+  if (P->q_len < 0) return -2;
   return 0;
 }
 
-/* Scaled scores of (b, h) for all its tokens: s[0 .. L_b). */
+/* Scaled scores of (b, v) for all of the request's tokens: s[0 .. L_b)
+ * (no causal cut: the caller reads the ones it needs). */
 int orc_scores(const orc_problem *P, const uint16_t *q, const uint16_t *k,
                const int32_t *page_table, const int32_t *seq_lens, int32_t b,
                int32_t h, double *s) {
@@ -204,15 +225,17 @@ int orc_scores(const orc_problem *P, const uint16_t *q, const uint16_t *k,
   return 0;
 }
 
-/* Full decode for every (b, h): out [B, Hq, Dv], lse [B, Hq]. */
+/* Full decode for every (b, v): out [B, q_len * Hq, Dv] (= [B, q_len, Hq,
+ * Dv]), lse [B, q_len * Hq]. */
 int orc_decode(const orc_problem *P, const uint16_t *q, const uint16_t *k,
                const uint16_t *v, const int32_t *page_table,
                const int32_t *seq_lens, double *out, double *lse) {
   int rc = check_problem(P);
   if (rc) return rc;
+  int VH = q_len_of(P) * P->heads;
   for (int b = 0; b < P->batch; ++b)
-    for (int h = 0; h < P->heads; ++h) {
-      int64_t i = (int64_t)b * P->heads + h;
+    for (int h = 0; h < VH; ++h) {
+      int64_t i = (int64_t)b * VH + h;
       rc = attend_range(P, q, k, v, page_table, seq_lens, b, h, 0, seq_lens[b],
                         out + i * P->head_dim_v, lse + i);
       if (rc) return rc;
@@ -220,8 +243,8 @@ int orc_decode(const orc_problem *P, const uint16_t *q, const uint16_t *k,
   return 0;
 }
 
-/* Decode for a list of (b, h) pairs: pairs[2i] = b, pairs[2i+1] = h; results
- * go to out[i * Dv ...] and lse[i]. */
+/* Decode for a list of (b, v) pairs: pairs[2i] = b, pairs[2i+1] = v (query
+ * token v / Hq, head v % Hq); results go to out[i * Dv ...] and lse[i]. */
 int orc_decode_pairs(const orc_problem *P, const uint16_t *q, const uint16_t *k,
                      const uint16_t *v, const int32_t *page_table,
                      const int32_t *seq_lens, const int32_t *pairs,
@@ -237,7 +260,7 @@ int orc_decode_pairs(const orc_problem *P, const uint16_t *q, const uint16_t *k,
   return 0;
 }
 
-/* One split's normalised partial over tokens [t0, t1) of (b, h). */
+/* One split's normalised partial over tokens [t0, t1) of (b, v). */
 int orc_partial(const orc_problem *P, const uint16_t *q, const uint16_t *k,
                 const uint16_t *v, const int32_t *page_table,
                 const int32_t *seq_lens, int32_t b, int32_t h, int64_t t0,
@@ -281,7 +304,7 @@ typedef struct {
   const uint16_t *q, *k, *v;
   const int32_t *page_table, *seq_lens;
   double *out, *lse;
-  int64_t first, last; /* pair range [first, last) in (b, h) order */
+  int64_t first, last; /* pair range [first, last) in (b, v) order */
   int rc;
 } orc_job;
 
@@ -289,8 +312,9 @@ static void *orc_worker(void *arg) {
   orc_job *J = (orc_job *)arg;
   const orc_problem *P = J->P;
   J->rc = 0;
+  int VH = q_len_of(P) * P->heads;
   for (int64_t i = J->first; i < J->last && !J->rc; ++i) {
-    int b = (int)(i / P->heads), h = (int)(i % P->heads);
+    int b = (int)(i / VH), h = (int)(i % VH);
     J->rc = attend_range(P, J->q, J->k, J->v, J->page_table, J->seq_lens, b, h,
                          0, J->seq_lens[b], J->out + i * P->head_dim_v,
                          J->lse + i);
@@ -304,7 +328,7 @@ int orc_decode_threads(const orc_problem *P, const uint16_t *q,
                        int32_t nthreads, double *out, double *lse) {
   int rc = check_problem(P);
   if (rc) return rc;
-  int64_t npairs = (int64_t)P->batch * P->heads;
+  int64_t npairs = (int64_t)P->batch * q_len_of(P) * P->heads;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > npairs) nthreads = (int32_t)(npairs > 0 ? npairs : 1);
   orc_job *jobs = (orc_job *)calloc((size_t)nthreads, sizeof(orc_job));

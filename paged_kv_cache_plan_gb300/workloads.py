@@ -15,7 +15,8 @@ Recipe (the same for every workload):
     V is the first 512 elements of the same row, page size 1.
 
 Layouts (all contiguous):
-  q          [B, Hq, D]
+  q          [B, Hq, D]; with q_len > 1 query tokens per request
+             [B, q_len, Hq, D] (the request's last q_len positions)
   k_pages    [P, Hkv, ps, k_row_pitch]      (MLA: [P, 1, 1, 576])
   v_pages    [P, Hkv, ps, v_row_pitch]      (MLA: the same tensor as k_pages)
   page_table [B, max_pages] int32
@@ -53,6 +54,7 @@ class DecodeCase:
     splits: int = 0
     unique_rows: int = 0          # distinct KV rows the batch reads (per KV head)
     meta: dict = field(default_factory=dict)
+    q_len: int = 1                # query tokens per request (last positions)
 
     @property
     def batch(self) -> int:
@@ -90,7 +92,7 @@ class DecodeCase:
                           self.seq_lens.to(device), self.heads, self.kv_heads,
                           self.head_dim, self.head_dim_v, self.page_size,
                           self.k_row_pitch, self.v_row_pitch, self.scale, self.dtype,
-                          self.mla, self.splits, self.unique_rows, dict(self.meta))
+                          self.mla, self.splits, self.unique_rows, dict(self.meta), self.q_len)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -114,9 +116,11 @@ def _randn(shape, g: torch.Generator, dtype: str, chunk_rows: int = 1 << 16) -> 
 def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
              page_size: int, seq_lens: Sequence[int], pool_pages: Optional[int] = None,
              dtype: str = "bf16", seed: int = 0, splits: int = 0,
-             scale: Optional[float] = None, name: str = "gqa") -> DecodeCase:
+             scale: Optional[float] = None, name: str = "gqa",
+             q_len: int = 1) -> DecodeCase:
     """GQA decode: Hq query heads over Hkv KV heads (consecutive groups),
-    HND pages [P, Hkv, ps, D], a seeded random page scatter."""
+    HND pages [P, Hkv, ps, D], a seeded random page scatter; q_len query
+    tokens per request."""
     lens = [int(x) for x in seq_lens]
     assert len(lens) == batch
     g = _gen(seed)
@@ -124,7 +128,8 @@ def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
     need = sum(npages)
     P = need if pool_pages is None else int(pool_pages)
     assert P >= need, "pool too small for the requested contexts"
-    q = _randn((batch, heads, head_dim), g, dtype)
+    q = _randn((batch, heads, head_dim) if q_len == 1 else (batch, q_len, heads, head_dim),
+               g, dtype)
     k = _randn((max(P, 1), kv_heads, page_size, head_dim), g, dtype)
     v = _randn((max(P, 1), kv_heads, page_size, head_dim), g, dtype)
     perm = torch.randperm(max(P, 1), generator=g).to(torch.int32)
@@ -137,13 +142,13 @@ def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
     return DecodeCase(name, q, k, v, pt, torch.tensor(lens, dtype=torch.int32), heads,
                       kv_heads, head_dim, head_dim, page_size, head_dim, head_dim,
                       float(scale if scale is not None else 1.0 / math.sqrt(head_dim)),
-                      dtype, False, splits, unique_rows=sum(lens))
+                      dtype, False, splits, unique_rows=sum(lens), q_len=q_len)
 
 
 def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
              group: int = 8, pool_rows: Optional[int] = None, dtype: str = "bf16",
              seed: int = 0, splits: int = 0, scale: Optional[float] = None,
-             name: str = "mla") -> DecodeCase:
+             name: str = "mla", q_len: int = 1) -> DecodeCase:
     """MLA decode: one 576-wide latent row (512 + 64) per token shared by all
     heads, page size 1. Requests in consecutive groups of ``group`` share the
     physical rows of their first ``prefix_len`` tokens; the rest are private.
@@ -155,7 +160,7 @@ def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
     unique = ngroups * prefix_len + batch * (seq_len - prefix_len)
     R = unique if pool_rows is None else int(pool_rows)
     assert R >= unique, "pool too small"
-    q = _randn((batch, heads, D), g, dtype)
+    q = _randn((batch, heads, D) if q_len == 1 else (batch, q_len, heads, D), g, dtype)
     perm = torch.randperm(R, generator=g).to(torch.int64)
     pt = torch.empty((batch, seq_len), dtype=torch.int64)
     nxt = 0
@@ -179,7 +184,7 @@ def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
     return DecodeCase(name, q, pool, pool, pt.to(torch.int32),
                       torch.full((batch,), seq_len, dtype=torch.int32), heads, 1, D, DV,
                       1, D, D, float(scale if scale is not None else 1.0 / math.sqrt(D)),
-                      dtype, True, splits, unique_rows=unique, meta=meta)
+                      dtype, True, splits, unique_rows=unique, meta=meta, q_len=q_len)
 
 
 # ---------------------------------------------------------------------------
@@ -258,7 +263,7 @@ def permute_pages(case: DecodeCase, seed: int) -> DecodeCase:
                       case.seq_lens, case.heads, case.kv_heads, case.head_dim,
                       case.head_dim_v, case.page_size, case.k_row_pitch, case.v_row_pitch,
                       case.scale, case.dtype, case.mla, case.splits, case.unique_rows,
-                      dict(case.meta))
+                      dict(case.meta), case.q_len)
 
 
 def oracle_problem_kwargs(case: DecodeCase) -> dict:
@@ -267,4 +272,4 @@ def oracle_problem_kwargs(case: DecodeCase) -> dict:
                 head_dim=case.head_dim, head_dim_v=case.head_dim_v,
                 page_size=case.page_size, dtype=case.dtype, max_pages=case.max_pages,
                 k_row_pitch=case.k_row_pitch, v_row_pitch=case.v_row_pitch,
-                scale=case.scale)
+                scale=case.scale, q_len=case.q_len)

@@ -18,6 +18,10 @@ What pins what:
   * relabelling     -- permuting physical pages changes nothing (bit-exact)
   * split + merge   -- any split of the tokens, merged, equals the one-shot
                        result (aiter pull 4758, Technical Details 3)
+  * several query tokens -- token j of q_len equals a one-token decode of the
+                       request cut to its first L - q_len + j + 1 tokens
+                       (bit-exact), and torch fp64 with an explicit causal
+                       mask on the gathered rows
 """
 import math
 
@@ -250,9 +254,62 @@ def pin_pairs_and_threads(mutation=0):
     assert np.array_equal(to, out) and np.array_equal(tl, lse)
 
 
+def _truncated(case, j):
+    """One-token problem of query token j: the requests cut to L - q_len + j + 1
+    tokens (same pages), q = token j's rows."""
+    lens = (case.seq_lens - case.q_len + j + 1).clamp(min=0).to(torch.int32)
+    return W.DecodeCase(case.name + f"_tok{j}", case.q[:, j].contiguous(), case.k_pages,
+                        case.v_pages, case.page_table, lens, case.heads, case.kv_heads,
+                        case.head_dim, case.head_dim_v, case.page_size, case.k_row_pitch,
+                        case.v_row_pitch, case.scale, case.dtype, case.mla, case.splits,
+                        case.unique_rows, dict(case.meta), 1)
+
+
+def _multi_token_cases():
+    gqa = W.gqa_case(batch=3, heads=4, kv_heads=2, head_dim=8, page_size=4,
+                     seq_lens=[13, 3, 9], pool_pages=12, seed=31, q_len=3)
+    mla = W.mla_case(batch=2, heads=4, seq_len=7, prefix_len=4, group=2, pool_rows=40,
+                     seed=33, q_len=4)
+    D, DV = 24, 16   # narrowed rows, as in _small_mla
+    pool = mla.k_pages[..., :D].contiguous()
+    mla = W.DecodeCase("mla_small_q4", mla.q[..., :D].contiguous(), pool, pool,
+                       mla.page_table, mla.seq_lens, 4, 1, D, DV, 1, D, D,
+                       1.0 / math.sqrt(D), "bf16", True, 0, mla.unique_rows, {}, 4)
+    return [gqa, mla]
+
+
+def pin_multi_token_truncation(mutation=0):
+    for case in _multi_token_cases():
+        out, lse = _decode(case, mutation)
+        H = case.heads
+        assert out.shape == (case.batch, case.q_len * H, case.head_dim_v)
+        for j in range(case.q_len):
+            to, tl = _decode(_truncated(case, j), mutation)
+            assert np.array_equal(out[:, j * H:(j + 1) * H], to)
+            assert np.array_equal(lse[:, j * H:(j + 1) * H], tl)
+
+
+def pin_multi_token_library(mutation=0):
+    for case in _multi_token_cases():
+        out, lse = _decode(case, mutation)
+        g = case.heads // case.kv_heads
+        for b in range(case.batch):
+            L = int(case.seq_lens[b])
+            for j in range(case.q_len):
+                for h in range(case.heads):
+                    k, v = _rows(case, b, h // g)
+                    s = (k @ case.q[b, j, h].double()) * case.scale
+                    s[L - case.q_len + j + 1:] = -math.inf     # causal within the tokens
+                    vh = j * case.heads + h
+                    np.testing.assert_allclose(out[b, vh], (torch.softmax(s, 0) @ v).numpy(),
+                                               rtol=0, atol=1e-12)
+                    assert abs(lse[b, vh] - float(torch.logsumexp(s, 0))) < 1e-12
+
+
 PINS = [pin_decoders, pin_q_zero_mean, pin_single_key, pin_two_keys,
         pin_library_crosscheck, pin_head_groups, pin_relabelling, pin_split_merge,
-        pin_merge_closed_form, pin_empty_request, pin_pairs_and_threads]
+        pin_merge_closed_form, pin_empty_request, pin_pairs_and_threads,
+        pin_multi_token_truncation, pin_multi_token_library]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
