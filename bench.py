@@ -374,8 +374,8 @@ def main():
     if plan.info["num_prefix_items"] > 0:
         vname = "mla_tc"   # the shared-prefix items dominate
     kernel_src = os.path.join(ROOT, "paged_kv_cache_plan_gb300", "csrc",
-                              {"mla_tc": "stage1_mla_tc.cu", "mla_mma": "stage1_mla.cu"}.get(
-                                  vname, "stage1_gqa.cu"))
+                              {"mla_tc": "stage1_mla_tc.cu", "mla_mma": "stage1_mla.cu",
+                               "gqa_fma": "stage1_gqa_fma.cu"}.get(vname, "stage1_gqa_mma.cu"))
     traffic = recorded_traffic(kernel_src, case.name)
     clocks = clk.summary()
 

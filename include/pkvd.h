@@ -1,17 +1,23 @@
 /*
  * pkvd.h -- paged-KV split-KV decode attention on GB300 (sm_103a): C ABI.
  *
- * One new query token per request is scored against that request's paged KV
- * cache. The work is cut into splits along the sequence; each split runs an
- * online softmax over its tokens and leaves a normalised P.V partial with its
- * log-sum-exp, and a second kernel merges the splits of every (request,
- * head). The operation is
+ * The new query token(s) of each request are scored against that request's
+ * paged KV cache. The work is cut into splits along the sequence; each split
+ * runs an online softmax over its tokens and leaves a normalised P.V partial
+ * with its log-sum-exp, and a second kernel merges the splits of every
+ * (request, query token, head). With one query token per request the
+ * operation is
  *
  *     out[b,h,:] = sum_t softmax_t(scale * q[b,h,:] . K[row(b,t,kv),:]) * V[row(b,t,kv),:Dv]
  *     lse[b,h]   = ln sum_t exp(scale * q[b,h,:] . K[row(b,t,kv),:])
  *
- * with kv = h / (heads / kv_heads) and row(b,t,kv) = (page_table[b][t/ps] *
- * kv_heads + kv) * ps + t % ps. Sources for the pieces:
+ * over t = 0 .. L_b - 1, with kv = h / (heads / kv_heads) and row(b,t,kv) =
+ * (page_table[b][t/ps] * kv_heads + kv) * ps + t % ps. With q_len > 1 query
+ * tokens per request (draft tokens verified in one step), the request's last
+ * q_len positions are its queries, already written to the cache: query token
+ * j (0-based) sits at position L_b - q_len + j and its sums run over
+ * t = 0 .. L_b - q_len + j only (causal among the new tokens). Sources for
+ * the pieces:
  *   - the split policy, the split-major grid and the head-dim-tiled merge:
  *     aiter pull 4758, "[Gluon][MLA] Deeper async-copy pipeline in the bh16
  *     stage-1 decode loop", Motivation and Technical Details 1-3;
@@ -29,12 +35,12 @@
  *        576-wide row (pass v_pages == k_pages, both row pitches equal).
  *
  * Layouts (row-major, contiguous unless a pitch says otherwise):
- *   q          [batch, heads, head_dim]                   bf16 or fp16
+ *   q          [batch, q_len, heads, head_dim]            bf16 or fp16
  *   k_pages    [num_pool_pages, kv_heads, page_size, k_row_pitch]
  *   v_pages    [num_pool_pages, kv_heads, page_size, v_row_pitch]
  *   page_table [batch, max_pages_per_seq]                  int32 page ids
- *   out        [batch, heads, head_dim_v]                  fp32
- *   lse        [batch, heads]                              fp32, natural log
+ *   out        [batch, q_len, heads, head_dim_v]           fp32
+ *   lse        [batch, q_len, heads]                       fp32, natural log
  * Every device pointer must be 16-byte aligned, and each row pitch times the
  * element size a multiple of 16 bytes.
  *
@@ -120,7 +126,12 @@ typedef struct pkvd_plan_desc {
   int32_t num_sms;            /* 0 = query the device                             */
   int32_t ctas_per_sm;        /* 0 = query the occupancy of the chosen kernel     */
   int32_t min_chunk;          /* 0 = default: smallest split, in tokens           */
-  int32_t reserved;           /* must be 0                                        */
+  int32_t q_len;              /* query tokens per request, 0 = 1; at most 8. Every
+                                 non-empty request needs L_b >= q_len. GQA: the
+                                 mma variant with q_len * heads / kv_heads <= 16
+                                 (the FMA variant takes q_len 1 only); MLA: both
+                                 variants (tensor-memory: q_len * heads a
+                                 multiple of 64); no shared-prefix plans          */
   int64_t max_pages_per_seq;  /* page_table row stride; 0 = max ceil(L_b / ps)    */
   int64_t num_pool_pages;     /* pages in the pools; 0 = unknown (no checks)      */
   int64_t k_row_pitch;        /* elements between K rows; 0 = D (MLA: 576)        */
@@ -138,7 +149,7 @@ typedef struct pkvd_plan_info {
   int32_t stage2_threads;     /* threads per merge block                          */
   int32_t num_sms;            /* SMs the plan fills                               */
   int32_t ctas_per_sm;        /* resident stage-1 blocks per SM                   */
-  int32_t heads_per_unit;     /* query heads one stage-1 item covers              */
+  int32_t heads_per_unit;     /* (query token, head) rows one stage-1 item covers */
   int32_t units_per_request;  /* stage-1 items per (request, split)               */
   int32_t num_items;          /* stage-1 grid size                                */
   int32_t num_partial_rows;   /* sum over requests of their split counts          */
@@ -169,7 +180,8 @@ typedef struct pkvd_work_item {
                                  the 64 query rows, `split` their prefix split,
                                  partial_row unused (each member's row is its
                                  first partial row + split); else 0              */
-  int32_t reserved1;
+  int32_t query_pos;          /* L_b - q_len: query token j of the request sees the
+                                 tokens t <= query_pos + j                       */
 } pkvd_work_item;
 
 /* GQA shorthand of decode_plan_ex (head_dim_v = head_dim, bf16, all other

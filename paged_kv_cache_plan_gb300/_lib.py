@@ -28,7 +28,7 @@ class PlanDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "heads", "kv_heads", "head_dim", "head_dim_v", "page_size", "dtype",
         "splits", "grid_order", "stage2_tiles", "variant", "checks", "num_sms",
-        "ctas_per_sm", "min_chunk", "reserved")] + [
+        "ctas_per_sm", "min_chunk", "q_len")] + [
         (n, ctypes.c_int64) for n in ("max_pages_per_seq", "num_pool_pages",
                                       "k_row_pitch", "v_row_pitch")] + [
         ("scale", ctypes.c_float), ("reserved2", ctypes.c_int32)]
@@ -51,7 +51,7 @@ class PlanInfo(ctypes.Structure):
 class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "request", "unit", "split", "partial_row", "tok_begin", "tok_end",
-        "grouped", "reserved1")]
+        "grouped", "query_pos")]
 
 
 # Every function the header declares, with (restype, argtypes).

@@ -32,7 +32,7 @@ def make_desc(batch: int, heads: int, kv_heads: int, head_dim: int, page_size: i
               stage2_tiles: int = 0, variant: str = "auto", checks: bool = False,
               num_sms: int = 0, ctas_per_sm: int = 0, min_chunk: int = 0,
               max_pages_per_seq: int = 0, num_pool_pages: int = 0, k_row_pitch: int = 0,
-              v_row_pitch: int = 0, scale: float = 0.0) -> PlanDesc:
+              v_row_pitch: int = 0, scale: float = 0.0, q_len: int = 0) -> PlanDesc:
     d = PlanDesc()
     d.batch, d.heads, d.kv_heads, d.head_dim = batch, heads, kv_heads, head_dim
     d.head_dim_v, d.page_size, d.dtype = head_dim_v, page_size, _DTYPES[dtype]
@@ -41,6 +41,7 @@ def make_desc(batch: int, heads: int, kv_heads: int, head_dim: int, page_size: i
     d.num_sms, d.ctas_per_sm, d.min_chunk = num_sms, ctas_per_sm, min_chunk
     d.max_pages_per_seq, d.num_pool_pages = max_pages_per_seq, num_pool_pages
     d.k_row_pitch, d.v_row_pitch, d.scale = k_row_pitch, v_row_pitch, scale
+    d.q_len = q_len
     return d
 
 
@@ -170,12 +171,13 @@ def _check_tensors(plan: Plan, q, k_pages, v_pages, page_table, out, lse) -> Non
             raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    if tuple(q.shape) != (d.batch, d.heads, d.head_dim):
-        raise ValueError(f"q shape {tuple(q.shape)} != {(d.batch, d.heads, d.head_dim)}")
-    if tuple(out.shape) != (d.batch, d.heads, dv):
-        raise ValueError(f"out shape {tuple(out.shape)} != {(d.batch, d.heads, dv)}")
-    if tuple(lse.shape) != (d.batch, d.heads):
-        raise ValueError(f"lse shape {tuple(lse.shape)} != {(d.batch, d.heads)}")
+    # one query token: [B, Hq, ...]; q_len > 1: [B, q_len, Hq, ...]
+    tok = () if d.q_len <= 1 else (d.q_len,)
+    for name, t, want in (("q", q, (d.batch, *tok, d.heads, d.head_dim)),
+                          ("out", out, (d.batch, *tok, d.heads, dv)),
+                          ("lse", lse, (d.batch, *tok, d.heads))):
+        if tuple(t.shape) != want:
+            raise ValueError(f"{name} shape {tuple(t.shape)} != {want}")
     if page_table.dim() != 2 or page_table.shape[0] != d.batch:
         raise ValueError("page_table must be [batch, max_pages_per_seq]")
 
@@ -212,6 +214,8 @@ def plan_for_case(case, *, shared_prefix: bool = False, **kw) -> Plan:
     """Plan matching a workloads.DecodeCase (splits from the case unless
     given). shared_prefix: use the case's prefix groups (decode_plan_prefix)."""
     kw.setdefault("splits", 0 if shared_prefix else case.splits)
+    if case.q_len != 1:
+        kw.setdefault("q_len", case.q_len)
     desc = make_desc(case.batch, case.heads, case.kv_heads, case.head_dim, case.page_size,
                      head_dim_v=case.head_dim_v, dtype=case.dtype,
                      max_pages_per_seq=case.max_pages, num_pool_pages=case.pool_pages,
@@ -227,11 +231,13 @@ def run_case(plan: Plan, case_dev, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, stream=None):
     """Run a plan on a DecodeCase whose tensors are on the GPU; returns (out, lse)."""
     dev = case_dev.q.device
+    tok = () if case_dev.q_len == 1 else (case_dev.q_len,)
     if out is None:
-        out = torch.empty((case_dev.batch, case_dev.heads, case_dev.head_dim_v),
+        out = torch.empty((case_dev.batch, *tok, case_dev.heads, case_dev.head_dim_v),
                           dtype=torch.float32, device=dev)
     if lse is None:
-        lse = torch.empty((case_dev.batch, case_dev.heads), dtype=torch.float32, device=dev)
+        lse = torch.empty((case_dev.batch, *tok, case_dev.heads), dtype=torch.float32,
+                          device=dev)
     decode_run(plan, case_dev.q, case_dev.k_pages, case_dev.v_pages, case_dev.page_table,
                out, lse, stream)
     return out, lse

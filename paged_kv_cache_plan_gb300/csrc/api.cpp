@@ -86,6 +86,7 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
     a.v_pitch = d.v_row_pitch;
     a.num_pool_pages = d.num_pool_pages;
     a.heads = d.heads;
+    a.q_len = d.q_len;
     a.kv_heads = d.kv_heads;
     a.page_size = d.page_size;
     a.dv = d.head_dim_v;
@@ -114,12 +115,12 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
   m.split_base = p->d_split_base;
   m.out = out;
   m.lse = lse;
-  m.heads = d.heads;
+  m.heads = d.q_len * d.heads;
   m.dv = d.head_dim_v;
   m.tiles = L.info.stage2_tiles;
   void* margs[] = {&m};
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(d.batch * d.heads), static_cast<unsigned>(m.tiles));
+  cfg.gridDim = dim3(static_cast<unsigned>(d.batch * m.heads), static_cast<unsigned>(m.tiles));
   cfg.blockDim = dim3(static_cast<unsigned>(L.info.stage2_threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(p->s2_smem);
   cfg.stream = stream;
@@ -178,7 +179,7 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, seq_lens), &s1))
     return PKVD_EUNSUPPORTED;
   if (prefix) {
-    if (family != PKVD_FAMILY_MLA || !pkvd::mla_tc_kernel(d.dtype, &s1p)) return PKVD_EUNSUPPORTED;
+    if (family != PKVD_FAMILY_MLA || !pkvd::mla_tc_kernel(d.dtype, false, &s1p)) return PKVD_EUNSUPPORTED;
     if (cudaFuncSetAttribute(s1p.func, cudaFuncAttributeMaxDynamicSharedMemorySize, s1p.smem) !=
         cudaSuccess)
       return PKVD_ECUDA;
@@ -221,7 +222,8 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   }
   p->device = dev;
   const pkvd::PlanLayout& L = p->layout;
-  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.heads, L.desc.head_dim_v, &s2)) {
+  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.q_len * L.desc.heads,
+                           L.desc.head_dim_v, &s2)) {
     delete p;   // the plan's merge shape and the kernel table disagree
     return PKVD_EUNSUPPORTED;
   }
@@ -242,8 +244,8 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   const size_t n_items = L.items.size() + L.prefix_items.size();
   const size_t b_items = al(std::max<size_t>(n_items, 1) * sizeof(pkvd_work_item));
   const size_t b_split = al(static_cast<size_t>(L.desc.batch + 1) * 4);
-  const size_t b_opart = al(rows * L.desc.heads * L.desc.head_dim_v * 4);
-  const size_t b_lpart = al(rows * L.desc.heads * 4);
+  const size_t b_opart = al(rows * L.desc.q_len * L.desc.heads * L.desc.head_dim_v * 4);
+  const size_t b_lpart = al(rows * L.desc.q_len * L.desc.heads * 4);
   const size_t b_status = al(16);
   p->dbytes = b_items + b_split + b_opart + b_lpart + b_status;
   if (cudaMalloc(&p->dmem, p->dbytes) != cudaSuccess) {

@@ -115,6 +115,9 @@ constexpr int kMlaTcSmemBytes = kTileAlign + kMlaTcQBytes + kMlaTcStages * kMlaT
 // output tolerance.
 constexpr int kMlaTcMinContext = 1024;
 
+// Query tokens per request a plan takes (multi-token decode).
+constexpr int kMaxQueryLen = 8;
+
 // Stage 2 keeps one float4 sum per warp (8 warps) and float4 column of its
 // Dv slice in shared memory.
 constexpr int kMaxSplits = 8192;

@@ -31,6 +31,8 @@ struct Stage1Args {
   int32_t kv_heads;              // Hkv
   int32_t page_size;             // tokens per page
   int32_t dv;                    // Dv
+  int32_t q_len;                 // query tokens per request: q is [B, q_len, Hq, D] and
+                                 // the partials hold q_len * Hq rows per split
   float scale_log2;              // scale * log2(e): scores go straight to exp2
   int32_t checks;                // 1 = bounds-check page ids
 };
@@ -38,12 +40,12 @@ struct Stage1Args {
 // Arguments of the merge kernel (one block per (request, head, Dv slice)).
 struct Stage2Args {
   const float* o_part;
-  const float* lse_part;         // [Hq, lse_stride]
+  const float* lse_part;         // [q_len * Hq, lse_stride]
   int64_t lse_stride;
   const int32_t* split_base;     // [B + 1] first partial row of each request
-  float* out;                    // [B, Hq, Dv]
-  float* lse;                    // [B, Hq] natural log
-  int32_t heads;
+  float* out;                    // [B, q_len * Hq, Dv]
+  float* lse;                    // [B, q_len * Hq] natural log
+  int32_t heads;                 // q_len * Hq (query token, head) rows
   int32_t dv;
   int32_t tiles;                 // Dv slices (gridDim.y)
 };
@@ -67,9 +69,11 @@ struct KernelEntry {
 
 // Lookups; false when the combination has no kernel.
 bool gqa_fma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
-bool gqa_mma_kernel(int dtype, int head_dim, int group, bool tiles, KernelEntry* e);
-bool mla_mma_kernel(int dtype, KernelEntry* e);
-bool mla_tc_kernel(int dtype, KernelEntry* e);
+// cols = q_len x group; causal: several query tokens per request (a cut per
+// (query token, head) row); the one-token kernels have none.
+bool gqa_mma_kernel(int dtype, int head_dim, int cols, bool tiles, bool causal, KernelEntry* e);
+bool mla_mma_kernel(int dtype, bool causal, KernelEntry* e);
+bool mla_tc_kernel(int dtype, bool causal, KernelEntry* e);
 // The merge kernel of a plan (threads and shared memory filled in): one
 // thread per column when no request has more than kMergeColMaxSplits
 // splits; otherwise split-parallel, with deep prefetch when the merge grid

@@ -14,12 +14,17 @@
 namespace pkvd {
 
 bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e) {
+  // a GQA item covers the q_len x group (query token, head) rows of a KV head
+  const int q_len = d.q_len > 0 ? d.q_len : 1;
   const int group = d.heads / d.kv_heads;
+  const bool causal = q_len > 1;
   switch (d.variant) {
-    case PKVD_VARIANT_GQA_FMA: return gqa_fma_kernel(d.dtype, d.head_dim, group, tiles, e);
-    case PKVD_VARIANT_GQA_MMA: return gqa_mma_kernel(d.dtype, d.head_dim, group, tiles, e);
-    case PKVD_VARIANT_MLA_MMA: return !tiles && mla_mma_kernel(d.dtype, e);
-    case PKVD_VARIANT_MLA_TC: return !tiles && mla_tc_kernel(d.dtype, e);
+    case PKVD_VARIANT_GQA_FMA:
+      return !causal && gqa_fma_kernel(d.dtype, d.head_dim, group, tiles, e);
+    case PKVD_VARIANT_GQA_MMA:
+      return gqa_mma_kernel(d.dtype, d.head_dim, q_len * group, tiles, causal, e);
+    case PKVD_VARIANT_MLA_MMA: return !tiles && mla_mma_kernel(d.dtype, causal, e);
+    case PKVD_VARIANT_MLA_TC: return !tiles && mla_tc_kernel(d.dtype, causal, e);
     default: return false;
   }
 }

@@ -80,7 +80,9 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
       d.min_chunk < 0 || d.max_pages_per_seq < 0 || d.num_pool_pages < 0 ||
       d.k_row_pitch < 0 || d.v_row_pitch < 0)
     return PKVD_EINVAL;
-  if (d.reserved != 0 || d.reserved2 != 0) return PKVD_EINVAL;
+  if (d.reserved2 != 0 || d.q_len < 0) return PKVD_EINVAL;
+  if (d.q_len == 0) d.q_len = 1;
+  if (d.q_len > kMaxQueryLen) return PKVD_EUNSUPPORTED;
   if (d.dtype != PKVD_BF16 && d.dtype != PKVD_FP16) return PKVD_EINVAL;
   if (d.grid_order < PKVD_ORDER_AUTO || d.grid_order > PKVD_ORDER_REQUEST_MAJOR)
     return PKVD_EINVAL;
@@ -114,25 +116,29 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
   int64_t max_pages = 0;
   for (int b = 0; b < d.batch; ++b) {
     if (seq_lens[b] < 0) return PKVD_EINVAL;
+    if (seq_lens[b] > 0 && seq_lens[b] < d.q_len) return PKVD_EINVAL;   // queries are cached tokens
     max_pages = std::max<int64_t>(max_pages, ceil_div(seq_lens[b], d.page_size));
   }
   if (d.max_pages_per_seq == 0) d.max_pages_per_seq = std::max<int64_t>(1, max_pages);
   if (d.max_pages_per_seq < max_pages) return PKVD_EINVAL;
 
+  // (query token, head) rows: a unit of the MLA kernels takes 16 or 64 of
+  // them; a GQA unit (one KV head) takes the q_len x group rows of its heads
   const int group = d.heads / d.kv_heads;
+  const int vheads = d.q_len * d.heads;
   if (mla) {
     if (d.variant == PKVD_VARIANT_AUTO) {
-      // tensor-memory kernel for 64-head blocks over long contexts, where
+      // tensor-memory kernel for 64-row blocks over long contexts, where
       // its one-part P rounding averages out (see kMlaTcMinContext)
       int64_t min_len = INT64_MAX;
       for (int b = 0; b < d.batch; ++b) min_len = std::min<int64_t>(min_len, seq_lens[b]);
-      d.variant = d.heads % kMlaTcHeads == 0 && min_len >= kMlaTcMinContext
+      d.variant = vheads % kMlaTcHeads == 0 && min_len >= kMlaTcMinContext
                       ? PKVD_VARIANT_MLA_TC
                       : PKVD_VARIANT_MLA_MMA;
     }
     if (d.variant != PKVD_VARIANT_MLA_MMA && d.variant != PKVD_VARIANT_MLA_TC)
       return PKVD_EUNSUPPORTED;
-    if (d.variant == PKVD_VARIANT_MLA_TC && d.heads % kMlaTcHeads != 0) return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_MLA_TC && vheads % kMlaTcHeads != 0) return PKVD_EUNSUPPORTED;
   } else {
     // The mma consumer is faster than the fp32 FMA consumer on every group
     // size measured on GB300 (the FMA path is issue-bound: about five
@@ -140,9 +146,11 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
     if (d.variant == PKVD_VARIANT_AUTO) d.variant = PKVD_VARIANT_GQA_MMA;
     if (d.variant != PKVD_VARIANT_GQA_FMA && d.variant != PKVD_VARIANT_GQA_MMA)
       return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_GQA_FMA && d.q_len != 1) return PKVD_EUNSUPPORTED;
   }
   VariantShape vs;
-  if (!variant_shape(d.variant, d.head_dim, group, false, &vs)) return PKVD_EUNSUPPORTED;
+  if (!variant_shape(d.variant, d.head_dim, d.q_len * group, false, &vs))
+    return PKVD_EUNSUPPORTED;
   *out = d;
   *family = mla ? PKVD_FAMILY_MLA : PKVD_FAMILY_GQA;
   return PKVD_OK;
@@ -157,9 +165,10 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
 
   const int B = d.batch;
   const int group = d.heads / d.kv_heads;
+  const int vheads = d.q_len * d.heads;     // merge rows per request
   const bool kv_tiles = plan_uses_tiles(d, seq_lens);
   VariantShape vs;
-  variant_shape(d.variant, d.head_dim, group, kv_tiles, &vs);
+  variant_shape(d.variant, d.head_dim, d.q_len * group, kv_tiles, &vs);
   const int blk = vs.block_tokens;
 
   PlanLayout& P = *out;
@@ -177,9 +186,9 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   I.ctas_per_sm = d.ctas_per_sm;
   if (family == PKVD_FAMILY_MLA) {
     I.heads_per_unit = d.variant == PKVD_VARIANT_MLA_TC ? kMlaTcHeads : kMlaHeads;
-    I.units_per_request = d.heads / I.heads_per_unit;
+    I.units_per_request = vheads / I.heads_per_unit;
   } else {
-    I.heads_per_unit = group;
+    I.heads_per_unit = d.q_len * group;
     I.units_per_request = d.kv_heads;
   }
   I.block_tokens = blk;
@@ -265,6 +274,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
     w.partial_row = P.split_base[b] + s;
     w.tok_begin = static_cast<int32_t>(s * chunk[b]);
     w.tok_end = static_cast<int32_t>(std::min<int64_t>(P.seq_lens[b], (s + 1) * chunk[b]));
+    w.query_pos = P.seq_lens[b] - d.q_len;
     P.items.push_back(w);
   };
   if (order == PKVD_ORDER_SPLIT_MAJOR) {
@@ -282,7 +292,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   // --- merge tiling
   const int dv = d.head_dim_v;
   int tiles = d.stage2_tiles;
-  const int64_t base = static_cast<int64_t>(B) * d.heads;
+  const int64_t base = static_cast<int64_t>(B) * vheads;
   if (tiles == 0) {
     tiles = 1;
     while (tiles < 8 && base * tiles * 2 <= d.num_sms && dv % (tiles * 2 * 32) == 0) tiles *= 2;
@@ -298,8 +308,8 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   I.workspace_bytes = al(static_cast<int64_t>(std::max<size_t>(P.items.size(), 1)) *
                          static_cast<int64_t>(sizeof(pkvd_work_item))) +
                       al(static_cast<int64_t>(B + 1) * 4) +
-                      al(std::max<int64_t>(rows, 1) * d.heads * dv * 4) +
-                      al(std::max<int64_t>(rows, 1) * d.heads * 4) + al(16);
+                      al(std::max<int64_t>(rows, 1) * vheads * dv * 4) +
+                      al(std::max<int64_t>(rows, 1) * vheads * 4) + al(16);
   return PKVD_OK;
 }
 
@@ -315,6 +325,7 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
   int family = 0;
   int nrc = normalise_desc(in, seq_lens, &nd, &family);
   if (nrc != PKVD_OK) return nrc;
+  if (nd.q_len != 1) return PKVD_EUNSUPPORTED;   // one query token per shared-prefix request
   if (in.heads < 1 || kMlaTcHeads % in.heads != 0 || in.heads % kMlaHeads != 0)
     return PKVD_EUNSUPPORTED;
   const int per_unit = kMlaTcHeads / in.heads;   // requests whose heads fill 64 rows
@@ -390,6 +401,7 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
     w.partial_row = base[w.request] + sp[w.request] + w.split;
     w.tok_begin += plen[w.request];
     w.tok_end += plen[w.request];
+    w.query_pos += plen[w.request];
   }
   for (int b = 0; b < B; ++b) P.splits[b] = sp[b] + P.splits[b];
   P.split_base = base;
@@ -409,6 +421,7 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
         w.partial_row = -1;
         w.tok_begin = static_cast<int32_t>(s * Cp);
         w.tok_end = static_cast<int32_t>(std::min<int64_t>(g.len, (s + 1) * Cp));
+        w.query_pos = static_cast<int32_t>(g.len - 1);   // every shared token is visible
         w.grouped = 1;
         P.prefix_items.push_back(w);
       }

@@ -35,7 +35,9 @@ constexpr int kPageWindow = 8;   // blocks of page ids read ahead
 // __syncthreads that also ORs a flag over the block.
 __device__ __forceinline__ bool block_sync_or(bool flag) { return __syncthreads_or(flag) != 0; }
 
-template <typename T>
+// CAUSAL: several query tokens per request (q_len > 1), each row cut at its
+// token's position; the one-token kernel has no per-row cut.
+template <typename T, bool CAUSAL>
 __global__ void __launch_bounds__(kMlaThreads, 2)
     mla_mma(const __grid_constant__ Stage1Args a, const __grid_constant__ KvTensorMaps) {
   constexpr int BLK = kMlaBlockTokens;
@@ -119,11 +121,14 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
   }
   int issued = min(nblk, STAGES);
 
-  // Q fragments of this warp's nine k-steps, heads g and g + 8.
+  // Q fragments of this warp's nine k-steps, rows g and g + 8 of the
+  // item's 16 (query token, head) rows unit * 16 .. unit * 16 + 15 (row v of
+  // a request is query token v / heads, head v % heads).
+  const int VH = a.q_len * a.heads;
   uint32_t qf[KSW][4];
   {
     const T* qg = static_cast<const T*>(a.q) +
-                  (static_cast<int64_t>(it.request) * a.heads + it.unit * HB) * kMlaDk;
+                  (static_cast<int64_t>(it.request) * VH + it.unit * HB) * kMlaDk;
 #pragma unroll
     for (int i = 0; i < KSW; ++i) {
       const int d = (warp * KSW + i) * 16 + 2 * t;
@@ -139,7 +144,11 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
   for (int i = 0; i < NTO; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};   // heads g, g + 8 (same in every warp)
+  float m_run[2] = {-INFINITY, -INFINITY};   // rows g, g + 8 (same in every warp)
+  // last visible token of rows g, g + 8, relative to the item
+  const int lim[2] = {CAUSAL ? it.query_pos + (it.unit * HB + g) / a.heads - it.tok_begin : 0,
+                      CAUSAL ? it.query_pos + (it.unit * HB + g + 8) / a.heads - it.tok_begin
+                             : 0};
   float l_run[2] = {0.f, 0.f};               // this lane's keys only
 
   // ldmatrix row addresses: K rows (keys) for the B operand of S, and V rows
@@ -197,8 +206,11 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
             rows[(i + STAGES - 1) % PF] = row_of(j + STAGES - 1 + PF);
           }
 
-          // Full scores: the four partials in warp order.
+          // Full scores: the four partials in warp order. Keys at or past
+          // kl[r] are past the item's end or not yet visible to row r.
           const int nv = min(BLK, n - j * BLK);
+          const int kl[2] = {CAUSAL ? min(nv, lim[0] - j * BLK + 1) : nv,
+                             CAUSAL ? min(nv, lim[1] - j * BLK + 1) : nv};
           float sc[2][4];
           float lm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -216,17 +228,19 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int key = nt * 8 + 2 * t + (e & 1);
-              sc[nt][e] = key < nv ? v[e] * a.scale_log2 : -INFINITY;
+              sc[nt][e] = key < kl[e >> 1] ? v[e] * a.scale_log2 : -INFINITY;
               lm[e >> 1] = fmaxf(lm[e >> 1], sc[nt][e]);
             }
           }
-          float alpha[2];
+          float alpha[2], m_ref[2];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             lm[r] = fmaxf(lm[r], __shfl_xor_sync(kFull, lm[r], 1));
             lm[r] = fmaxf(lm[r], __shfl_xor_sync(kFull, lm[r], 2));
             const float m_new = fmaxf(m_run[r], lm[r]);
-            alpha[r] = exp2f(m_run[r] - m_new);
+            // a row with no visible token yet keeps m = -inf, p = 0
+            m_ref[r] = CAUSAL && m_new == -INFINITY ? 0.f : m_new;
+            alpha[r] = exp2f(m_run[r] - m_ref[r]);
             m_run[r] = m_new;
           }
           // P in the A-operand layout: rows g / g + 8, keys 2t, 2t+1 (n-tile
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
             float p[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              p[e] = exp2f(sc[nt][e] - m_run[e >> 1]);
+              p[e] = exp2f(sc[nt][e] - m_ref[e >> 1]);
               psum[e >> 1] += p[e];
             }
             const uint32_t h0 = pack2<T>(p[0], p[1]), h1 = pack2<T>(p[2], p[3]);
@@ -292,7 +306,7 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
     l_run[r] += __shfl_xor_sync(kFull, l_run[r], 1);
     l_run[r] += __shfl_xor_sync(kFull, l_run[r], 2);
   }
-  const int64_t row0 = static_cast<int64_t>(it.partial_row) * a.heads + it.unit * HB;
+  const int64_t row0 = static_cast<int64_t>(it.partial_row) * VH + it.unit * HB;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int h = g + 8 * r;
@@ -311,9 +325,13 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
 
 }  // namespace
 
-bool mla_mma_kernel(int dtype, KernelEntry* e) {
-  e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_mma<__half>)
-                               : reinterpret_cast<const void*>(&mla_mma<__nv_bfloat16>);
+bool mla_mma_kernel(int dtype, bool causal, KernelEntry* e) {
+  if (causal)
+    e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_mma<__half, true>)
+                                 : reinterpret_cast<const void*>(&mla_mma<__nv_bfloat16, true>);
+  else
+    e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_mma<__half, false>)
+                                 : reinterpret_cast<const void*>(&mla_mma<__nv_bfloat16, false>);
   e->threads = kMlaThreads;
   e->smem = kMlaSmemBytes;
   e->block_tokens = kMlaBlockTokens;

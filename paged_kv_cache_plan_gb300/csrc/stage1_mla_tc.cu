@@ -59,6 +59,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLazyRescale = 8.f;   // log2 units
+// Reference maximum of a row that sees no token of its item's first block
+// (several query tokens: the causal cut). Finite, so P = exp2(-inf - m) = 0
+// and a later raise scales the (zero) row by exp2(floor - m) = 0.
+constexpr float kNoTokenMax = -1e30f;
 constexpr int kSlabs = kMlaDk / 64;   // 9
 
 // Byte offset, in a tile of 64-column slabs of `slab_bytes` each, of 16-byte
@@ -97,7 +101,9 @@ __device__ __forceinline__ void fold16(float (&v)[32], int lane) {
   fold_step<2, MAX>(v, 1, lane & 1);
 }
 
-template <typename T>
+// CAUSAL: several query tokens per request (q_len > 1), each row cut at its
+// token's position; the one-token kernel has no per-row cut.
+template <typename T, bool CAUSAL>
 __global__ void __launch_bounds__(kMlaTcThreads, 1)
     mla_tc(const __grid_constant__ Stage1Args a, const __grid_constant__ KvTensorMaps) {
   constexpr int R = kMlaTcHeads;              // 64 heads = N of both products
@@ -157,17 +163,20 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // Query row r of the item: head unit * 64 + r of the request, or (grouped
+  // (query token, head) rows of a request: row v is query token v / heads,
+  // head v % heads (grouped shared-prefix items have one query token)
+  const int VH = a.q_len * a.heads;
+  // Query row r of the item: row unit * 64 + r of the request, or (grouped
   // shared-prefix item) head r % heads of member r / heads; -1 for the unused
   // rows of a group with fewer members than fit.
   auto q_row = [&](int r) -> int64_t {
-    if (!it.grouped) return static_cast<int64_t>(it.request) * a.heads + it.unit * R + r;
+    if (!it.grouped) return static_cast<int64_t>(it.request) * VH + it.unit * R + r;
     const int m = r / a.heads;
     return m < it.unit ? static_cast<int64_t>(it.request + m) * a.heads + (r - m * a.heads) : -1;
   };
   // Partial-output row of query row r (-1: unused).
   auto out_row = [&](int r) -> int64_t {
-    if (!it.grouped) return static_cast<int64_t>(it.partial_row) * a.heads + it.unit * R + r;
+    if (!it.grouped) return static_cast<int64_t>(it.partial_row) * VH + it.unit * R + r;
     const int m = r / a.heads;
     return m < it.unit
                ? static_cast<int64_t>(a.split_base[it.request + m] + it.split) * a.heads +
@@ -338,13 +347,28 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     // running sums of P for this lane's key slot, per head, in the free
     // tensor-memory columns 384 + 32h .. (registers are the scarce resource)
     const uint32_t lcols = tbase + lanes + 6 * R + 32 * h;
-    // this lane's scaled scores of block j (keys past the end: -inf)
+    // Causal cut among the query tokens: row c of this warp's 32 sees the
+    // item's tokens up to vis0 + (query token of the row); blocks that end at
+    // or before vis0 need no per-row test (all of them, with one token).
+    const int vis0 = it.query_pos - it.tok_begin;
+    const int row0 = it.grouped ? 0 : it.unit * R + 32 * h;   // first row of this warp
+    // this lane's scaled scores of block j (keys past the end or not yet
+    // visible to the row: -inf)
     auto scores = [&](int j, int b, float (&x)[32]) {
       uint32_t r[32];
       tc::ld32(tbase + lanes + 4 * R + b * R + 32 * h, r);
       const bool valid = lane < 16 && key < min(BLK, n - j * BLK);
+      if (!CAUSAL || (j + 1) * BLK - 1 <= vis0) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) x[c] = valid ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+        for (int c = 0; c < 32; ++c) x[c] = valid ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+      } else {
+        const int kj = j * BLK + key;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int tok_j = it.grouped ? 0 : (row0 + c) / a.heads;
+          x[c] = valid && kj <= vis0 + tok_j ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+        }
+      }
     };
     bool bad = false;
 
@@ -393,7 +417,9 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
             const float mo = m_ref[col];
             float mn = mo, al = 1.f;
             if (j == 0) {
-              mn = bm;
+              // a row that sees no token of the first block (causal cut)
+              // starts from a finite floor, so that P = exp2(-inf - m) = 0
+              mn = CAUSAL && bm == -INFINITY ? kNoTokenMax : bm;
             } else if (bm > mo + kLazyRescale) {
               mn = bm;
               al = ex2(mo - mn);
@@ -496,9 +522,10 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           for (int e = 0; e < 2; ++e) {
             const int col = 32 * h + 2 * cl + e;
             const float l = ((red[col] + red[64 + col]) + red[128 + col]) + red[192 + col];
-            alpha_s[col] = nblk > 0 ? 1.f / l : 0.f;
+            const bool seen = nblk > 0 && (!CAUSAL || l > 0.f);   // some token was visible
+            alpha_s[col] = seen ? 1.f / l : 0.f;
             const int64_t li = lse_idx(col);
-            if (li >= 0) a.lse_part[li] = nblk > 0 ? m_ref[col] + log2f(l) : -INFINITY;
+            if (li >= 0) a.lse_part[li] = seen ? m_ref[col] + log2f(l) : -INFINITY;
           }
         }
         named_sync(1, SMX);
@@ -537,9 +564,13 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
 
 }  // namespace
 
-bool mla_tc_kernel(int dtype, KernelEntry* e) {
-  e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_tc<__half>)
-                               : reinterpret_cast<const void*>(&mla_tc<__nv_bfloat16>);
+bool mla_tc_kernel(int dtype, bool causal, KernelEntry* e) {
+  if (causal)
+    e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_tc<__half, true>)
+                                 : reinterpret_cast<const void*>(&mla_tc<__nv_bfloat16, true>);
+  else
+    e->func = dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&mla_tc<__half, false>)
+                                 : reinterpret_cast<const void*>(&mla_tc<__nv_bfloat16, false>);
   e->threads = kMlaTcThreads;
   e->smem = kMlaTcSmemBytes;
   e->block_tokens = kMlaTcBlockTokens;

@@ -106,7 +106,8 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     return PKVD_ENOMEM;
   }
   if (rc != PKVD_OK) return rc;
-  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.heads, L.desc.head_dim_v, &s2))
+  if (!pkvd::stage2_kernel(L.info, L.desc.batch, L.desc.q_len * L.desc.heads,
+                           L.desc.head_dim_v, &s2))
     return PKVD_EUNSUPPORTED;   // the plan's merge shape and the kernel table disagree
   const bool any_work = L.info.num_items > 0;
   if (any_work && (!q || !k_pages || !v_pages || !page_table)) return PKVD_EINVAL;
@@ -121,8 +122,8 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   const size_t b_status = al(16);
   const size_t b_split = al(static_cast<size_t>(L.desc.batch + 1) * 4);
   const size_t b_items = al(std::max<size_t>(L.items.size(), 1) * sizeof(pkvd_work_item));
-  const size_t b_lpart = al(rows * L.desc.heads * 4);
-  const size_t b_opart = al(rows * L.desc.heads * L.desc.head_dim_v * 4);
+  const size_t b_lpart = al(rows * L.desc.q_len * L.desc.heads * 4);
+  const size_t b_opart = al(rows * L.desc.q_len * L.desc.heads * L.desc.head_dim_v * 4);
   if (b_status + b_split + b_items + b_lpart + b_opart > kStaticScratchBytes)
     return PKVD_ENOMEM;
 
@@ -162,6 +163,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     a.v_pitch = L.desc.v_row_pitch;
     a.num_pool_pages = L.desc.num_pool_pages;
     a.heads = L.desc.heads;
+    a.q_len = L.desc.q_len;
     a.kv_heads = L.desc.kv_heads;
     a.page_size = L.desc.page_size;
     a.dv = L.desc.head_dim_v;
@@ -184,12 +186,12 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   m.split_base = d_split;
   m.out = out;
   m.lse = lse;
-  m.heads = L.desc.heads;
+  m.heads = L.desc.q_len * L.desc.heads;
   m.dv = L.desc.head_dim_v;
   m.tiles = L.info.stage2_tiles;
   void* margs[] = {&m};
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(L.desc.batch * L.desc.heads),
+  cfg.gridDim = dim3(static_cast<unsigned>(L.desc.batch * m.heads),
                      static_cast<unsigned>(m.tiles));
   cfg.blockDim = dim3(static_cast<unsigned>(L.info.stage2_threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(s2.smem);

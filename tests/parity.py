@@ -39,17 +39,22 @@ def oracle_pairs(case, pairs):
 
 def run_gpu(case, dev_case=None, poison=True, **plan_kw):
     """Plan + run through the C ABI; out/lse start NaN-filled so that a head
-    the kernels skip cannot pass. Returns (out, lse, plan) on the host."""
+    the kernels skip cannot pass. Returns (out, lse, plan) on the host, as
+    [B, q_len * Hq, Dv] / [B, q_len * Hq] (the oracle's (token, head) rows)."""
     dev = dev_case if dev_case is not None else case.to("cuda")
     plan = plan_for_case(case, **plan_kw)
-    out = torch.full((case.batch, case.heads, case.head_dim_v),
+    tok = () if case.q_len == 1 else (case.q_len,)
+    out = torch.full((case.batch, *tok, case.heads, case.head_dim_v),
                      float("nan") if poison else 0.0, dtype=torch.float32, device="cuda")
-    lse = torch.full((case.batch, case.heads), float("nan") if poison else 0.0,
+    lse = torch.full((case.batch, *tok, case.heads), float("nan") if poison else 0.0,
                      dtype=torch.float32, device="cuda")
     run_case(plan, dev, out, lse)
     torch.cuda.synchronize()
     status = plan.last_device_status()
     assert status == 0, f"device status {status}"
+    vh = case.q_len * case.heads
+    out = out.reshape(case.batch, vh, case.head_dim_v)
+    lse = lse.reshape(case.batch, vh)
     return out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), plan
 
 
@@ -79,7 +84,7 @@ def check_case(case, ref=None, **plan_kw):
 
 def sample_pairs(case, n, seed=0):
     rng = np.random.default_rng(seed)
-    B, H = case.batch, case.heads
+    B, H = case.batch, case.q_len * case.heads
     pairs = {(0, 0), (B - 1, H - 1)}
     while len(pairs) < min(n, B * H):
         pairs.add((int(rng.integers(B)), int(rng.integers(H))))

@@ -288,3 +288,55 @@ def test_merge_block_shape_follows_prefix_splits(L):
         info, _, _ = _prefix_plan(B, 16, seq, [0] * B, plen)
         assert info["stage2_threads"] == _merge_threads(info["max_splits"],
                                                         512 // info["stage2_tiles"])
+
+
+# ---------------------------------------------------------------- several query tokens
+
+@pytest.mark.parametrize("args,seq,kw,code", [
+    ((2, 8, 2, 128, 16), [100, 2], dict(q_len=3), _lib.PKVD_EINVAL),     # L < q_len
+    ((1, 8, 2, 128, 16), [100], dict(q_len=-1), _lib.PKVD_EINVAL),
+    ((1, 8, 2, 128, 16), [100], dict(q_len=9), _lib.PKVD_EUNSUPPORTED),  # over 8 tokens
+    ((1, 16, 2, 128, 16), [100], dict(q_len=3), _lib.PKVD_EUNSUPPORTED), # 3 x group 8 > 16
+    ((1, 8, 2, 128, 16), [100], dict(q_len=2, variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),
+    ((1, 16, 1, 576, 1), [2048], dict(q_len=2, variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),
+])
+def test_query_token_errors(L, args, seq, kw, code):
+    with pytest.raises(_lib.PkvdError) as e:
+        _plan(*args, seq=seq, **kw)
+    assert e.value.code == code
+
+
+def test_query_tokens_layout(L):
+    # GQA: an item covers q_len x group (token, head) rows of one KV head
+    info, items = _plan(2, 8, 2, 128, 16, seq=[300, 0], q_len=2)
+    assert info["heads_per_unit"] == 8 and info["units_per_request"] == 2
+    assert all(it[6] == 300 - 2 for it in _items_full(L, (2, 8, 2, 128, 16), [300, 0], q_len=2))
+    # MLA: 16 heads x 4 tokens fill a 64-row tensor-memory item on long contexts
+    info, _ = _plan(3, 16, 1, 576, 1, seq=[4096] * 3, q_len=4)
+    assert info["variant"] == 4 and info["heads_per_unit"] == 64
+    assert info["units_per_request"] == 1
+    info, _ = _plan(3, 16, 1, 576, 1, seq=[4096] * 3, q_len=2)
+    assert info["variant"] == 3 and info["units_per_request"] == 2
+    # the merge runs over batch x q_len x heads rows: 1 x 4 x 16 = 64 rows tile 2 ways
+    info, _ = _plan(1, 16, 1, 576, 1, seq=[68000], q_len=4)
+    assert info["stage2_tiles"] == 2
+    # no shared-prefix plans with several query tokens
+    from paged_kv_cache_plan_gb300 import decode_plan_prefix_compute
+    with pytest.raises(_lib.PkvdError) as e:
+        decode_plan_prefix_compute(make_desc(2, 16, 1, 576, 1, num_sms=152, ctas_per_sm=2,
+                                             q_len=2), [3000, 3000], [0, 0], [2000, 2000])
+    assert e.value.code == _lib.PKVD_EUNSUPPORTED
+
+
+def _items_full(L, args, seq, **kw):
+    # every field of the work items, query_pos included
+    import ctypes
+    desc = make_desc(*args, num_sms=152, ctas_per_sm=1, **kw)
+    info = _lib.PlanInfo()
+    arr = (_lib.WorkItem * 4096)()
+    s = (ctypes.c_int32 * len(seq))(*seq)
+    rc = L.decode_plan_compute(ctypes.byref(desc), ctypes.cast(s, ctypes.c_void_p),
+                               ctypes.byref(info), ctypes.cast(arr, ctypes.c_void_p), 4096)
+    assert rc == 0
+    return [(w.request, w.unit, w.split, w.partial_row, w.tok_begin, w.tok_end, w.query_pos)
+            for w in arr[:info.num_items]]
