@@ -40,18 +40,24 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 def workload(name: str):
+    """A named workload; a trailing "_q<n>" asks for n query tokens per request
+    (multi-token decode, causal among them) on the same cache."""
     from paged_kv_cache_plan_gb300 import workloads as W
+    q_len = 1
+    base, sep, tail = name.rpartition("_q")
+    if sep and tail.isdigit():
+        name, q_len = base, int(tail)
     if name.startswith("gqa_long_"):
-        return W.gqa_long(int(name.split("_")[-1].rstrip("k")) * 1024)
+        return W.gqa_long(int(name.split("_")[-1].rstrip("k")) * 1024, q_len=q_len)
     if name == "gqa_tiny":
-        return W.gqa_tiny()
+        return W.gqa_tiny(q_len=q_len)
     if name.startswith("mla16_b"):
-        return W.mla16(int(name[len("mla16_b"):]))
+        return W.mla16(int(name[len("mla16_b"):]), q_len=q_len)
     if name.startswith("mla_h"):
         h, b = name[len("mla_h"):].split("_b")
-        return W.mla_many(int(h), int(b))
+        return W.mla_many(int(h), int(b), q_len=q_len)
     if name.startswith("gqa_varlen_"):
-        return W.gqa_varlen(name[len("gqa_varlen_"):])
+        return W.gqa_varlen(name[len("gqa_varlen_"):], q_len=q_len)
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -172,7 +178,7 @@ def oracle_sample_rate(case, budget_s: float, threads: int):
         c = W.DecodeCase(case.name, case.q, case.k_pages, case.v_pages, case.page_table, lens,
                          case.heads, case.kv_heads, case.head_dim, case.head_dim_v,
                          case.page_size, case.k_row_pitch, case.v_row_pitch, case.scale,
-                         case.dtype, case.mla)
+                         case.dtype, case.mla, 0, 0, {}, case.q_len)
         return c
 
     def op_bytes(c):
@@ -200,8 +206,9 @@ def oracle_sample_rate(case, budget_s: float, threads: int):
         if time.perf_counter() >= t_end:
             break
     gbs = op_bytes(c) * reps / total / 1e9
-    sample = (f"{c.name}: first {n} of {maxL} tokens per request, all {case.batch * case.heads} "
-              f"heads, {reps} runs, fp64 oracle on {threads} threads")
+    sample = (f"{c.name}: first {n} of {maxL} tokens per request, all "
+              f"{case.batch * case.q_len * case.heads} (request, token, head) rows, {reps} runs, "
+              f"fp64 oracle on {threads} threads")
     return gbs, total / reps, sample, n
 
 
@@ -221,7 +228,8 @@ def reference_arm(args, world, rank):
     lens = torch.clamp(case.seq_lens, max=n).to(torch.int32)
     c = W.DecodeCase(case.name, case.q, case.k_pages, case.v_pages, case.page_table, lens,
                      case.heads, case.kv_heads, case.head_dim, case.head_dim_v, case.page_size,
-                     case.k_row_pitch, case.v_row_pitch, case.scale, case.dtype, case.mla)
+                     case.k_row_pitch, case.v_row_pitch, case.scale, case.dtype, case.mla,
+                     0, 0, {}, case.q_len)
     P = oracle.problem(**W.oracle_problem_kwargs(c))
     for _ in range(args.warmup):
         oracle.decode(P, c.q, c.k_pages, c.v_pages, c.page_table, c.seq_lens, threads=threads)
@@ -282,11 +290,13 @@ def main():
     if args.splits >= 0:
         kw["splits"] = args.splits
     groups = [g for g in case.meta.get("prefix_group", []) if g >= 0]
-    shared_prefix = not args.no_prefix and any(groups.count(g) > 1 for g in set(groups))
+    shared_prefix = (not args.no_prefix and case.q_len == 1
+                     and any(groups.count(g) > 1 for g in set(groups)))
     plan = plan_for_case(case, shared_prefix=shared_prefix, **kw)
-    out = torch.empty((case.batch, case.heads, case.head_dim_v), dtype=torch.float32,
+    tok = () if case.q_len == 1 else (case.q_len,)
+    out = torch.empty((case.batch, *tok, case.heads, case.head_dim_v), dtype=torch.float32,
                       device="cuda")
-    lse = torch.empty((case.batch, case.heads), dtype=torch.float32, device="cuda")
+    lse = torch.empty((case.batch, *tok, case.heads), dtype=torch.float32, device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     evict = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -397,6 +407,7 @@ def main():
             "config": {"workload": case.name, "batch": case.batch, "heads": case.heads,
                        "kv_heads": case.kv_heads, "head_dim": case.head_dim,
                        "head_dim_v": case.head_dim_v, "page_size": case.page_size,
+                       "query_tokens": case.q_len,
                        "seq_lens": (case.seq_lens.tolist() if case.batch <= 16 else
                                     f"{case.batch} x {int(case.seq_lens[0])}"),
                        "kv_bytes_per_op": bytes_op,

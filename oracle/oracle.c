@@ -23,8 +23,9 @@
  * double precision; bf16 and fp16 inputs convert to double exactly.
  *
  * Several query tokens per request (q_len >= 1: draft tokens checked in one
- * step, as in the rocm-libraries page's served models that decode with
- * multi-token-prediction drafts). The request's last q_len tokens are its
+ * step; the TensorFold pull 1932 page serves its model with multi-token-
+ * prediction drafts, Receipt, and asks that drafted output equal undrafted
+ * output, Checklist). The request's last q_len tokens are its
  * queries, already in the cache: query token j (0-based) sits at position
  * L_b - q_len + j and attends to the keys at or before its own position,
  * t = 0 .. L_b - q_len + j. q is [B, q_len, Hq, D] and out / lse follow the

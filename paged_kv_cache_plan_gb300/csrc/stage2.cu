@@ -50,14 +50,17 @@ __device__ __forceinline__ void add_xor4(float4& v, int m) {
 // in increasing s. The four groups of a warp are added by a xor butterfly
 // over lane bits 3-4, the eight warps' sums in warp order. Each lane holds
 // kLseRegs lse values (lane-strided) and the weights of its first kLseRegs
-// own splits in registers; further splits are read as they come. kPre:
-// partials per thread (of its first column) loaded together with the lse
-// values, before the weights are known -- all of a thread's splits when
-// S <= 32 kPre -- and the number of partial loads in flight per thread after
-// that. Deep (8, 8) when the merge grid is small and latency-bound; shallow
-// (2, 2) when it is large, where registers would cost occupancy.
-template <int kPre, int kLseRegs>
-__global__ void __launch_bounds__(kMergeThreads, kPre > 2 ? 2 : 5)
+// own splits in registers; further splits are read as they come. A thread
+// takes kU of its columns (c, c + 8, ...) at a time with kPre of each
+// column's splits in flight, kU x kPre loads at once; those of its first
+// columns are issued together with the lse values, before the weights are
+// known. The grouping changes no addition: every column sums its splits in
+// the same order whatever kU, kPre and the tiling. Variants: <8, 8, 1> for
+// small grids of narrow slices (a tiled Dv: one column per thread), <4, 8, 4>
+// for small grids of wide rows, <2, 2, 4> and <2, 2, 1> for large grids,
+// where registers would cost occupancy.
+template <int kPre, int kLseRegs, int kU>
+__global__ void __launch_bounds__(kMergeThreads, kPre > 2 ? 2 : 3)
     merge_splits(const __grid_constant__ Stage2Args a) {
   static_assert(kLseRegs % kPre == 0, "prefetch depth divides the register window");
   extern __shared__ float4 wsum4[];   // [kWarps][C4] warp sums
@@ -82,17 +85,19 @@ __global__ void __launch_bounds__(kMergeThreads, kPre > 2 ? 2 : 5)
   const int64_t stride = static_cast<int64_t>(a.heads) * a.dv;
   const float* base = a.o_part + (static_cast<int64_t>(r0) * a.heads + h) * a.dv + d0;
   const float* lp = a.lse_part + h * a.lse_stride + r0;   // this head's splits
+  auto part = [&](int s, int c) {   // partial of split s, float4 column c (0 past the ends)
+    return c < C4 && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
 
-  // One round trip: the first kPre partials of this thread's first column,
-  // and the lse values (lane-strided, for M and the weight sum; and those of
-  // this thread's own splits grp + 32 i).
-  float4 pre[kPre];
+  // One round trip: the first kPre partials of this thread's first kU
+  // columns (x holds the loads in flight), and the lse values (lane-strided,
+  // for M and the weight sum; and those of this thread's own splits grp + 32 i).
+  float4 x[kU][kPre];
 #pragma unroll
-  for (int u = 0; u < kPre; ++u) {
-    const int s = grp + u * kSplitGroups;
-    pre[u] = ct < C4 && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + ct)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  for (int u = 0; u < kU; ++u)
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) x[u][j] = part(grp + j * kSplitGroups, u * kColThreads + ct);
   float lv[kLseRegs], lo[kLseRegs];
 #pragma unroll
   for (int i = 0; i < kLseRegs; ++i) {
@@ -124,36 +129,39 @@ __global__ void __launch_bounds__(kMergeThreads, kPre > 2 ? 2 : 5)
 #pragma unroll
   for (int i = 0; i < kLseRegs; ++i) wo[i] = weight(lo[i]);
 
-  for (int c0 = 0; c0 < C4; c0 += kColThreads) {
-    const int c = c0 + ct;
-    const bool valid = c < C4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // own splits below 32 kLseRegs, kPre loads in flight at a time (the
-    // terms past S are zero, so stopping there changes no bits)
+  for (int c0 = 0; c0 < C4; c0 += kColThreads * kU) {
+    float4 acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // own splits below 32 kLseRegs (the terms past S are zero, so stopping
+    // there changes no bits)
 #pragma unroll
     for (int i0 = 0; i0 < kLseRegs; i0 += kPre) {
       if (grp + kSplitGroups * i0 >= S) break;
-      float4 x[kPre];
+      if (i0 > 0 || c0 > 0) {   // the first chunk was loaded before the weights
 #pragma unroll
-      for (int j = 0; j < kPre; ++j) {
-        const int s = grp + kSplitGroups * (i0 + j);
-        if (i0 == 0 && c0 == 0)
-          x[j] = pre[j];
-        else
-          x[j] = valid && s < S ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int j = 0; j < kPre; ++j)
+            x[u][j] = part(grp + kSplitGroups * (i0 + j), c0 + u * kColThreads + ct);
       }
 #pragma unroll
-      for (int j = 0; j < kPre; ++j) fma4(acc, wo[i0 + j], x[j]);
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int j = 0; j < kPre; ++j) fma4(acc[u], wo[i0 + j], x[u][j]);
     }
     for (int s = grp + kSplitGroups * kLseRegs; s < S; s += kSplitGroups) {
-      const float l = __ldg(lp + s);
-      fma4(acc, weight(l), valid ? __ldg(reinterpret_cast<const float4*>(base + s * stride) + c)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f));
+      const float w = weight(__ldg(lp + s));
+#pragma unroll
+      for (int u = 0; u < kU; ++u) fma4(acc[u], w, part(s, c0 + u * kColThreads + ct));
     }
-    add_xor4(acc, 8);
-    add_xor4(acc, 16);
-    if (lane < kColThreads && valid) wsum4[warp * C4 + c] = acc;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = c0 + u * kColThreads + ct;
+      add_xor4(acc[u], 8);
+      add_xor4(acc[u], 16);
+      if (lane < kColThreads && c < C4) wsum4[warp * C4 + c] = acc[u];
+    }
   }
   __syncthreads();
   float* out = a.out + static_cast<int64_t>(bh) * a.dv + d0;
@@ -257,8 +265,11 @@ bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, Ker
     e->smem = 0;
   } else {
     const bool deep = static_cast<int64_t>(batch) * heads * tiles <= 2LL * info.num_sms;
-    e->func = deep ? reinterpret_cast<const void*>(&merge_splits<8, 8>)
-                   : reinterpret_cast<const void*>(&merge_splits<2, 2>);
+    const bool wide = dv / tiles / 4 > kColThreads;   // several columns per thread
+    e->func = deep ? (wide ? reinterpret_cast<const void*>(&merge_splits<4, 8, 4>)
+                           : reinterpret_cast<const void*>(&merge_splits<8, 8, 1>))
+                   : (wide ? reinterpret_cast<const void*>(&merge_splits<2, 2, 4>)
+                           : reinterpret_cast<const void*>(&merge_splits<2, 2, 1>));
     e->threads = kMergeThreads;
     e->smem = stage2_smem_bytes(dv / tiles);
   }

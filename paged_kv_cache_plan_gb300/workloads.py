@@ -199,25 +199,29 @@ VARLEN_LENS = (256, 512, 768, 1024, 1536, 2048, 8192, 32768, 65536, 131072)
 VARLEN_POOL_PAGES = 300_000 // 16  # a pool sized for 300K tokens
 
 
-def gqa_tiny(seed: int = 1001) -> DecodeCase:
+def _qsuffix(q_len: int) -> str:
+    return "" if q_len == 1 else f"_q{q_len}"
+
+
+def gqa_tiny(seed: int = 1001, q_len: int = 1) -> DecodeCase:
     """Batch 1, 4 query heads on 1 KV head, d 128, 512 tokens, page 16,
     32 pages shuffled in a pool of 32, 4 KV splits."""
     return gqa_case(batch=1, heads=4, kv_heads=1, head_dim=128, page_size=16,
                     seq_lens=[512], pool_pages=32, seed=seed, splits=4,
-                    name="gqa_tiny_b1_h4kv1_d128_L512")
+                    name="gqa_tiny_b1_h4kv1_d128_L512" + _qsuffix(q_len), q_len=q_len)
 
 
-def gqa_long(context: int, seed: Optional[int] = None) -> DecodeCase:
+def gqa_long(context: int, seed: Optional[int] = None, q_len: int = 1) -> DecodeCase:
     """Batch 1, 16 query heads over 2 KV heads (group 8), d 256, page 16,
     pool = context/16 pages in random order."""
     return gqa_case(batch=1, heads=16, kv_heads=2, head_dim=256, page_size=16,
                     seq_lens=[context], seed=1002 + context if seed is None else seed,
-                    name=f"gqa_long_b1_h16kv2_d256_L{context}")
+                    name=f"gqa_long_b1_h16kv2_d256_L{context}" + _qsuffix(q_len), q_len=q_len)
 
 
 def mla16(batch: int, seed: Optional[int] = None, context: int = MLA16_CONTEXT,
           prefix: int = MLA16_PREFIX, pool_rows: int = MLA16_POOL_ROWS,
-          splits: Optional[int] = None) -> DecodeCase:
+          splits: Optional[int] = None, q_len: int = 1) -> DecodeCase:
     """16 heads on one 576-wide latent row, page 1, 68,000-token contexts whose
     first 63,240 tokens are shared by groups of 8, a 2,000,000-row pool
     (over 2 GiB, so 64-bit offsets), splits = 256 // batch."""
@@ -225,27 +229,29 @@ def mla16(batch: int, seed: Optional[int] = None, context: int = MLA16_CONTEXT,
                     group=8, pool_rows=pool_rows,
                     seed=1003 + batch if seed is None else seed,
                     splits=max(1, 256 // batch) if splits is None else splits,
-                    name=f"mla16_b{batch}_L{context}_prefix{prefix}")
+                    name=f"mla16_b{batch}_L{context}_prefix{prefix}" + _qsuffix(q_len),
+                    q_len=q_len)
 
 
 def mla_many(heads: int, batch: int, seed: Optional[int] = None,
-             context: int = MLA_MANY_CONTEXT) -> DecodeCase:
+             context: int = MLA_MANY_CONTEXT, q_len: int = 1) -> DecodeCase:
     """nhead 64/128 on the 576-wide latent row, page 1, 16,384 distinct
     tokens per request."""
     return mla_case(batch=batch, heads=heads, seq_len=context, prefix_len=0,
                     seed=1004 + heads + batch if seed is None else seed,
-                    name=f"mla_h{heads}_b{batch}_L{context}")
+                    name=f"mla_h{heads}_b{batch}_L{context}" + _qsuffix(q_len), q_len=q_len)
 
 
 def gqa_varlen(dtype: str = "bf16", seed: Optional[int] = None,
                lens: Sequence[int] = VARLEN_LENS,
-               pool_pages: Optional[int] = VARLEN_POOL_PAGES) -> DecodeCase:
+               pool_pages: Optional[int] = VARLEN_POOL_PAGES, q_len: int = 1) -> DecodeCase:
     """Batch 10, 32 query heads over 8 KV heads, d 128, page 16, the varlen
     context mix, pages scattered over a 300K-token pool."""
     return gqa_case(batch=len(lens), heads=32, kv_heads=8, head_dim=128,
                     page_size=16, seq_lens=list(lens), pool_pages=pool_pages,
                     dtype=dtype, seed=(1005 if dtype == "bf16" else 1105) if seed is None else seed,
-                    name=f"gqa_varlen_{dtype}_b{len(lens)}_h32kv8_d128")
+                    name=f"gqa_varlen_{dtype}_b{len(lens)}_h32kv8_d128" + _qsuffix(q_len),
+                    q_len=q_len)
 
 
 def permute_pages(case: DecodeCase, seed: int) -> DecodeCase:
