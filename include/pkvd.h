@@ -248,6 +248,18 @@ int decode_plan_query(const pkvd_plan *plan, pkvd_plan_info *info);
  * PKVD_OK, PKVD_EDEVICE_CHECK or PKVD_ETIMEOUT. */
 int decode_last_device_status(const pkvd_plan *plan, pkvd_stream_t stream);
 
+/* Self-test of the kernels' bounded pipeline waits. Launches one block on
+ * `stream` that waits, through the same bounded barrier wait the stage-1
+ * kernels use, on a shared-memory barrier that nothing completes, with a
+ * limit of limit_us microseconds (1 .. 10,000,000). The wait runs out; the
+ * block writes status[0] = PKVD_ETIMEOUT (PKVD_OK would mean the barrier
+ * completed, PKVD_ECUDA that the wait gave up before its limit) and
+ * status[1] = the microseconds it waited, then exits: nothing hangs or
+ * faults, and the context stays usable. status: caller-owned device array
+ * of two int32. Asynchronous; returns PKVD_EINVAL for a bad argument,
+ * PKVD_ECUDA if the launch failed. */
+int decode_selftest_wait_timeout(int32_t *status, int64_t limit_us, pkvd_stream_t stream);
+
 /* The split planner alone, on the host, with no CUDA call: desc->num_sms and
  * desc->ctas_per_sm must be set (> 0). Fills *info and, when `items` is not
  * NULL, up to `capacity` work items in grid order. Returns PKVD_OK, or

@@ -75,6 +75,7 @@ SIGNATURES = {
                                                   ctypes.POINTER(PlanInfo), _vp, _i64]),
     "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
+    "decode_selftest_wait_timeout": (ctypes.c_int, [_vp, _i64, _vp]),
 }
 
 _lock = threading.Lock()

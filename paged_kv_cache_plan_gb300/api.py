@@ -210,6 +210,19 @@ def decode_run_timed(plan: Plan, q, k_pages, v_pages, page_table, out, lse, ev_b
                                       ctypes.c_void_p(s), *ev), "decode_run_timed")
 
 
+def selftest_wait_timeout(limit_us: int = 2000, stream=None):
+    """Run the bounded-wait self-test (decode_selftest_wait_timeout): a wait
+    that nothing completes must give up after limit_us. Returns (status,
+    microseconds waited)."""
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    check(_lib.lib().decode_selftest_wait_timeout(_ptr(st), int(limit_us), ctypes.c_void_p(s)),
+          "decode_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    v = st.cpu().tolist()
+    return int(v[0]), int(v[1])
+
+
 def plan_for_case(case, *, shared_prefix: bool = False, **kw) -> Plan:
     """Plan matching a workloads.DecodeCase (splits from the case unless
     given). shared_prefix: use the case's prefix groups (decode_plan_prefix)."""

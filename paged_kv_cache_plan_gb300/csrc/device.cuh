@@ -72,15 +72,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase of `parity` to complete; false when the wait ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `parity` to complete; false when the wait ran out
+// (after limit_ns, checked every 32 tries).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 31u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
     if (i == 0x40000000u) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // Non-blocking test of the phase of `parity`.
