@@ -254,6 +254,81 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def prefill_arm(args, world, rank, local):
+    """The second workload: dense causal prefill at head_dim 64, named
+    prefill_d64_b<B>_h<Hq>kv<Hkv>_L<L>. Times prefill_d64_run with CUDA events
+    after an L2 flush, and reports algorithmic TFLOP/s (causal: 4 x 64 x
+    L (L + 1) / 2 flops per request and head) against the measured bf16
+    tensor peak."""
+    import re
+    import torch
+    import numpy as np
+    from paged_kv_cache_plan_gb300 import build as _build
+    _build.build()
+    from paged_kv_cache_plan_gb300 import prefill_d64
+    from paged_kv_cache_plan_gb300 import workloads as W
+    m = re.fullmatch(r"prefill_d64_b(\d+)_h(\d+)kv(\d+)_L(\d+)", args.workload)
+    if not m:
+        raise SystemExit(f"unknown workload {args.workload}")
+    B, H, Hkv, L = (int(x) for x in m.groups())
+    torch.cuda.set_device(local)
+    case = W.prefill_case(batch=B, heads=H, kv_heads=Hkv, seq_len=L, seed=1006 + L)
+    q, k, v = case.q.cuda(), case.k_pages.cuda(), case.v_pages.cuda()
+    out = torch.empty((B, L, H, 64), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, L, H), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    evict = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        prefill_d64(q, k, v, out=out, lse=lse, status=status)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        evict.sum()
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for a, b in evs:
+            flush.fill_(1.0)
+            evict.sum()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    assert int(status.item()) == 0, "a pipeline wait ran out"
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evs])), world)
+    flops = 4.0 * 64 * L * (L + 1) / 2 * B * H
+    tflops = flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, src = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops)"
+    except Exception:
+        peak, src = 1900.0, "fallback"
+    line = {
+        "metric": "dense causal prefill TFLOP/s at head_dim 64 (second workload)",
+        "value": round(tflops * world, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": case.name, "batch": B, "heads": H, "kv_heads": Hkv,
+                   "seq_len": L, "head_dim": 64, "causal": True,
+                   "l2": "flushed before every step (512 MB write, then 512 MB read, outside the events)"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "prefill_d64", "peak_source": src},
+        "gpu_launches": args.steps, "clocks": clk.summary(), "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -273,6 +348,11 @@ def main():
     world, rank, local = dist_init()
     if args.impl == "reference":
         reference_arm(args, world, rank)
+        barrier(world)
+        return
+
+    if args.workload.startswith("prefill_d64_"):
+        prefill_arm(args, world, rank, local)
         barrier(world)
         return
 

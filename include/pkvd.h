@@ -248,6 +248,45 @@ int decode_plan_query(const pkvd_plan *plan, pkvd_plan_info *info);
  * PKVD_OK, PKVD_EDEVICE_CHECK or PKVD_ETIMEOUT. */
 int decode_last_device_status(const pkvd_plan *plan, pkvd_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Dense causal prefill attention, head_dim 64 (a second workload: the whole
+ * prompt at once instead of one decode step). Every token t of request b
+ * attends to that request's tokens 0 .. t:
+ *
+ *     out[b,t,h,:] = sum_{u<=t} softmax_u(scale * q[b,t,h,:] . k[b,kv,u,:]) * v[b,kv,u,:]
+ *     lse[b,t,h]   = ln sum_{u<=t} exp(scale * q[b,t,h,:] . k[b,kv,u,:])
+ *
+ * with kv = h / (heads / kv_heads). It is the multi-token decode above with
+ * q_len = seq_len on an unpaged cache (one page of seq_len tokens per
+ * request). The rocm-libraries pull 10102 page is about this kernel's
+ * shared-memory pitch at D = 64; here the tiles use the 128-byte TMA swizzle,
+ * which a 64-element row fills exactly (no pad needed).
+ *
+ * Layouts (contiguous, 16-byte aligned):
+ *   q    [batch, seq_len, heads, 64]       bf16 or fp16
+ *   k, v [batch, kv_heads, seq_len, 64]    same type
+ *   out  [batch, seq_len, heads, 64]       fp32
+ *   lse  [batch, seq_len, heads]           fp32, natural log
+ *   status  one caller-owned device int32: a pipeline wait that ran out ORs
+ *           in a nonzero bit (the caller zeroes it and reads it after a sync)
+ */
+typedef struct pkvd_prefill_desc {
+  int32_t batch;              /* requests, >= 1                                   */
+  int32_t heads;              /* query heads                                       */
+  int32_t kv_heads;           /* KV heads; heads % kv_heads == 0                   */
+  int32_t seq_len;            /* tokens per request, >= 1                          */
+  int32_t dtype;              /* pkvd_dtype                                        */
+  float scale;                /* 0 = 1 / 8 (= 1 / sqrt(64))                        */
+  int32_t reserved[2];        /* must be 0                                         */
+} pkvd_prefill_desc;
+
+/* Launch the prefill on `stream` (asynchronous, allocates nothing). Returns
+ * PKVD_EINVAL for a bad argument or pointer alignment, PKVD_EUNSUPPORTED for
+ * heads % kv_heads != 0 or a grid too large, PKVD_ECUDA if a tensor map or
+ * the launch failed. */
+int prefill_d64_run(const pkvd_prefill_desc *desc, const void *q, const void *k, const void *v,
+                    float *out, float *lse, int32_t *status, pkvd_stream_t stream);
+
 /* Self-test of the kernels' bounded pipeline waits. Launches one block on
  * `stream` that waits, through the same bounded barrier wait the stage-1
  * kernels use, on a shared-memory barrier that nothing completes, with a

@@ -9,8 +9,8 @@ library; the first call does, and fails loudly if it is not built.
 """
 from .api import (Plan, decode_plan, decode_plan_compute, decode_plan_ex, decode_plan_prefix,
                   decode_plan_prefix_compute, decode_run, decode_run_timed, make_desc,
-                  plan_for_case, run_case, selftest_wait_timeout)
+                  plan_for_case, prefill_d64, run_case, selftest_wait_timeout)
 
 __all__ = ["Plan", "decode_plan", "decode_plan_ex", "decode_plan_prefix", "decode_run",
            "decode_run_timed", "decode_plan_compute", "decode_plan_prefix_compute", "make_desc",
-           "plan_for_case", "run_case", "selftest_wait_timeout"]
+           "plan_for_case", "prefill_d64", "run_case", "selftest_wait_timeout"]

@@ -34,6 +34,14 @@ class PlanDesc(ctypes.Structure):
         ("scale", ctypes.c_float), ("reserved2", ctypes.c_int32)]
 
 
+class PrefillDesc(ctypes.Structure):
+    """pkvd_prefill_desc (include/pkvd.h)."""
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("kv_heads", ctypes.c_int32), ("seq_len", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32 * 2)]
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "family", "variant", "grid_order", "stage2_tiles", "stage2_threads", "num_sms",
@@ -76,6 +84,8 @@ SIGNATURES = {
     "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
     "decode_selftest_wait_timeout": (ctypes.c_int, [_vp, _i64, _vp]),
+    "prefill_d64_run": (ctypes.c_int, [ctypes.POINTER(PrefillDesc), _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _vp]),
 }
 
 _lock = threading.Lock()

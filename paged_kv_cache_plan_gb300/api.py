@@ -223,6 +223,45 @@ def selftest_wait_timeout(limit_us: int = 2000, stream=None):
     return int(v[0]), int(v[1])
 
 
+def prefill_d64(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float = 0.0,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None):
+    """Dense causal prefill attention at head_dim 64 (prefill_d64_run):
+    q [B, L, Hq, 64], k / v [B, Hkv, L, 64] (bf16 or fp16, contiguous, on the
+    GPU). Returns (out [B, L, Hq, 64] fp32, lse [B, L, Hq] fp32, status), with
+    status a device int32 that is nonzero if a pipeline wait ran out.
+    Asynchronous on ``stream``."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, L, Hq, 64] and k, v [B, Hkv, L, 64]")
+    B, L, H, D = q.shape
+    Hkv = k.shape[1]
+    if D != 64 or tuple(k.shape) != (B, Hkv, L, 64):
+        raise ValueError(f"shapes q {tuple(q.shape)}, k {tuple(k.shape)} do not match")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.device.type != "cuda" or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of q's dtype")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("bf16 or fp16 inputs")
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, L, H, 64), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, L, H), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if tuple(out.shape) != (B, L, H, 64) or tuple(lse.shape) != (B, L, H):
+        raise ValueError("out must be [B, L, Hq, 64] and lse [B, L, Hq]")
+    d = _lib.PrefillDesc()
+    d.batch, d.heads, d.kv_heads, d.seq_len = B, H, Hkv, L
+    d.dtype = _lib.PKVD_FP16 if q.dtype == torch.float16 else _lib.PKVD_BF16
+    d.scale = scale
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    check(_lib.lib().prefill_d64_run(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     _ptr(lse), _ptr(status), ctypes.c_void_p(s)),
+          "prefill_d64_run")
+    return out, lse, status
+
+
 def plan_for_case(case, *, shared_prefix: bool = False, **kw) -> Plan:
     """Plan matching a workloads.DecodeCase (splits from the case unless
     given). shared_prefix: use the case's prefix groups (decode_plan_prefix)."""

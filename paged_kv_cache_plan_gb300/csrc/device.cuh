@@ -176,6 +176,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// The same through a 4D tensor map.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(bar)
+      : "memory");
+}
+
 // Fetch a tensor map (a __grid_constant__ kernel parameter, by its generic
 // address) into the descriptor cache ahead of its first copy.
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -204,6 +215,13 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void pdl_wait_prerequisites() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// 2^x on the special-function unit (callers pass inputs <= 8 or -inf).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // --------------------------------------------------- tensor-core fragments

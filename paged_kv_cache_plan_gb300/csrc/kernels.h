@@ -83,6 +83,12 @@ bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, Ker
 // Stage-1 kernel for a normalised plan description (variant resolved).
 bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e);
 
+// A tiled tensor map with 128-byte swizzle over a 16-bit tensor: rank 2..5,
+// dims innermost first, strides[i] = bytes between steps of dim i + 1, box
+// the copied tile; out-of-range elements read as zero. Returns a pkvd_status.
+int encode_tiled_map(int dtype, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMap* out);
+
 // Encode the K and V tensor maps of the page-tile path for the given pool
 // pointers: {64 columns, pool rows, D/64 column blocks}, box {64, 16, D/64},
 // 128-byte swizzle. Returns a pkvd_status.

@@ -70,6 +70,27 @@ int encode_one(PFN_cuTensorMapEncodeTiled_v12000 fn, const pkvd_plan_desc& d, co
 
 }  // namespace
 
+int encode_tiled_map(int dtype, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMap* out) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return PKVD_ECUDA;
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bx[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bx[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = strides[i - 1];
+  }
+  const CUresult r =
+      fn(out, dtype == PKVD_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+         static_cast<cuuint32_t>(rank), const_cast<void*>(base), gdim, gstride, bx, estride,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKVD_OK : PKVD_ECUDA;
+}
+
 int encode_kv_maps(const pkvd_plan_desc& d, const void* k, const void* v, KvTensorMaps* out) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return PKVD_ECUDA;

@@ -1,0 +1,413 @@
+// Dense causal prefill attention at head_dim 64 (prefill_d64_run in
+// include/pkvd.h): every token of a prompt attends to the tokens at or before
+// it. The rocm-libraries pull 10102 page (Motivation, Technical Details) is
+// about this kernel's shared-memory layout at D = 64: there a 64-element row
+// is half of one DMA row group, a per-row pad cannot be placed, and the pad
+// goes between row groups to spread the LDS banks. Here a 64-element bf16 row
+// is exactly one 128-byte swizzle row, so every tile moves with TMA in the
+// canonical 128-byte-swizzled layout (16-byte chunk c of row r at
+// r * 128 + ((c ^ (r % 8)) * 16) within 1 KB atoms): eight consecutive rows
+// of a chunk land in eight distinct bank groups with no pad at all, and the
+// tensor cores read the tiles through descriptors.
+//
+// One block per (request, query head, 128-query tile); six warps:
+//   * warps 0-3: softmax, one query row per thread (tensor-memory lane =
+//     row); scores are read from tensor memory twice (block maximum, then P),
+//     P = exp2(s - m) goes to shared memory as a 16-bit high part plus the
+//     16-bit rounding of its remainder (two products, ~16 significant bits:
+//     the rows near a sequence's start have a handful of keys, where one
+//     rounding of P alone would not average out), running sums in fp32;
+//   * warp 4: TMA producer (the query tile once, then K and V tiles of 128
+//     keys through two stages);
+//   * warp 5: tensor-memory allocation and the MMA issue: S = Q K^T
+//     (M = 128 queries, N = 128 keys, K = 64) into one of two S buffers, then
+//     O += P V (M = 128, N = 64, K = 128 keys) for both parts of P.
+// The running maximum is lazy (raised only when a block's maximum exceeds it
+// by more than 2^8); a raise rescales the thread's O row in tensor memory
+// after the previous O product is complete. Causality: key tiles 0 .. qt of
+// query tile qt; the diagonal tile masks keys after the row's own position.
+// Every wait is bounded; a wait that runs out sets the status word, and every
+// role drains what it issued before the block frees its tensor memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "device.cuh"
+#include "kernels.h"
+#include "tcgen05.cuh"
+
+namespace pkvd {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int PD = 64;                 // head dim (K and V)
+constexpr int BM = 128;                // queries per block
+constexpr int BN = 128;                // keys per tile
+constexpr int TILE = BN * PD * 2;      // 16 KB: a Q, K or V tile
+constexpr int PSLAB = BM * 128;        // 16 KB: 128 rows x 64 keys of P
+constexpr int PPART = 2 * PSLAB;       // 32 KB: one part (high or low) of a P tile
+constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 4, kProducerWarp = 4, kMmaWarp = 5;
+constexpr float kLazyRescale = 8.f;    // log2 units
+constexpr uint32_t TCOLS = 512;        // S buffers at columns 0 and 128, O at 256
+constexpr int kOnePartFrom = 1024;     // query positions from which P is one 16-bit part
+
+// shared memory: [Q][K0][K1][V0][V1][P0 hi][P0 lo][P1 hi][P1 lo][misc]
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE;
+constexpr int OFF_V = OFF_K + 2 * TILE;
+constexpr int OFF_P = OFF_V + 2 * TILE;
+constexpr int OFF_MISC = OFF_P + 4 * PPART;
+constexpr int MISC = 256;
+constexpr int kPrefillSmem = 1024 + OFF_MISC + MISC;   // 1 KB alignment slack
+static_assert(kPrefillSmem <= 232448, "shared memory per block");
+
+struct PrefillArgs {
+  float* out;            // [B, L, Hq, 64]
+  float* lse;            // [B, L, Hq] natural log
+  int32_t* status;       // device status word (kStatus* bits)
+  int32_t batch, heads, kv_heads, seq_len;
+  int32_t q_tiles;       // ceil(L / 128)
+  float scale_log2;
+};
+
+struct PrefillMaps {
+  CUtensorMap q;         // {64, Hq, L, B}, box {64, 1, 128, 1}
+  CUtensorMap k;         // {64, L, B * Hkv}, box {64, 128, 1}
+  CUtensorMap v;
+};
+
+// byte offset of 16-byte chunk c (0..15: keys 8c .. 8c+7) of row r in a P part
+__device__ __forceinline__ uint32_t p_off(int r, int c) {
+  return (c >> 3) * PSLAB + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_d64(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr uint32_t kIdS = tc::idesc_f16(kBf16, BM, BN, false, false);
+  constexpr uint32_t kIdO = tc::idesc_f16(kBf16, BM, PD, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  uint8_t* misc = sm + OFF_MISC;
+  const uint32_t bars = smem_addr(misc);
+  const uint32_t qfull = bars, kvfull = bars + 8, kvempty = bars + 24, sfull = bars + 40,
+                 sfree = bars + 56, pfull = bars + 72, pfree = bars + 88, drain = bars + 104;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // heavy (late) query tiles first
+  const int bh_count = a.batch * a.heads;
+  const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / bh_count;
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int b = bh / a.heads, h = bh % a.heads;
+  const int kvh = h / (a.heads / a.kv_heads);
+  const int nkv = qt + 1;                      // key tiles 0 .. qt
+  // P in two 16-bit parts while some row of the tile has few keys (the rows
+  // of tiles at or past kOnePartFrom tokens see more than that many keys,
+  // where the rounding of a one-part P averages out)
+  const bool two_part = qt * BM < kOnePartFrom;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&maps.q);
+    tma_prefetch_desc(&maps.k);
+    tma_prefetch_desc(&maps.v);
+    mbar_init(qfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kvfull + 8 * i, 1);
+      mbar_init(kvempty + 8 * i, 1);
+      mbar_init(sfull + 8 * i, 1);
+      mbar_init(sfree + 8 * i, kSoftmaxWarps);
+      mbar_init(pfull + 8 * i, kSoftmaxWarps);
+      mbar_init(pfree + 8 * i, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tc::alloc(smem_addr(tslot), TCOLS);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicOr(a.status, kStatusTimeout);
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA
+    if (lane == 0) {
+      const int kvrow = b * a.kv_heads + kvh;
+      mbar_arrive_expect_tx(qfull, TILE);
+      tma_load_4d(smem_addr(sm + OFF_Q), &maps.q, 0, h, qt * BM, b, qfull);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && (*abort_flag || !mbar_wait(kvempty + 8 * s, ((j >> 1) - 1) & 1))) {
+          fail();
+          break;
+        }
+        mbar_arrive_expect_tx(kvfull + 8 * s, 2 * TILE);
+        tma_load_3d(smem_addr(sm + OFF_K + s * TILE), &maps.k, 0, j * BN, kvrow, kvfull + 8 * s);
+        tma_load_3d(smem_addr(sm + OFF_V + s * TILE), &maps.v, 0, j * BN, kvrow, kvfull + 8 * s);
+        issued = j + 1;
+      }
+      // copies still in flight must land before the block exits
+      mbar_wait(qfull, 0);
+      for (int j = (issued >= 2 ? issued - 2 : 0); j < issued; ++j)
+        mbar_wait(kvfull + 8 * (j & 1), (j >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint64_t dq = tc::sdesc(smem_addr(sm + OFF_Q), 16, 1024);          // K-major
+      const uint64_t dk0 = tc::sdesc(smem_addr(sm + OFF_K), 16, 1024);         // K-major
+      const uint64_t dv0 = tc::sdesc(smem_addr(sm + OFF_V), TILE, 1024);       // MN-major
+      const uint64_t dp0 = tc::sdesc(smem_addr(sm + OFF_P), 16, 1024);         // K-major
+      constexpr uint64_t kTileStep = TILE >> 4, kPartStep = PPART >> 4, kSlabStep = PSLAB >> 4;
+      const uint32_t tO = tbase + 256;
+      bool ok = mbar_wait(qfull, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1;
+        if (*abort_flag || !mbar_wait(kvfull + 8 * s, (j >> 1) & 1)) return false;
+        if (j >= 2 && (*abort_flag || !mbar_wait(sfree + 8 * s, ((j >> 1) - 1) & 1))) return false;
+        tc::fence_after();
+        const uint32_t d = tbase + s * BN;
+        const uint64_t dk = dk0 + s * kTileStep;
+#pragma unroll
+        for (int k = 0; k < PD / 16; ++k) tc::mma_f16(d, dq + 2 * k, dk + 2 * k, kIdS, k > 0);
+        tc::commit(sfull + 8 * s);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        const int s = j & 1;
+        if (*abort_flag || !mbar_wait(pfull + 8 * s, (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const uint64_t dv = dv0 + s * kTileStep;
+        const uint64_t dph = dp0 + s * 2 * kPartStep, dpl = dph + kPartStep;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint64_t koff = (k >> 2) * kSlabStep + (k & 3) * 2;
+          tc::mma_f16(tO, dph + koff, dv + k * (2048 >> 4), kIdO, j > 0 || k > 0);
+          if (two_part) tc::mma_f16(tO, dpl + koff, dv + k * (2048 >> 4), kIdO, true);
+        }
+        tc::commit(kvempty + 8 * s);
+        tc::commit(pfree + 8 * s);
+      }
+      if (!ok) fail();
+      // every product issued must be complete before the memory is freed
+      tc::commit(drain);
+      mbar_wait(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = threadIdx.x;                           // query row of this thread
+    const int qi = qt * BM + r;                          // its position
+    const uint32_t lanes = static_cast<uint32_t>(32 * warp) << 16;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool bad = false;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(kFull, !*abort_flag && mbar_wait(bar, parity));
+    };
+    for (int j = 0; j < nkv; ++j) {
+      const int s = j & 1;
+      if (!wait_all(sfull + 8 * s, (j >> 1) & 1)) {
+        bad = true;
+        break;
+      }
+      tc::fence_after();
+      // the row's 128 scaled scores, read once (keys after the row's own
+      // position masked on the diagonal tile)
+      const uint32_t ts = tbase + lanes + s * BN;
+      float sc[BN];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t x[32];
+        tc::ld32(ts + 32 * c4, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[32 * c4 + i] = __uint_as_float(x[i]) * sl2;
+      }
+      // S buffer s is in registers: the MMA may overwrite it
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree + 8 * s);
+      if (j == qt) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (j * BN + c > qi) sc[c] = -INFINITY;
+      }
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mb = fmaxf(mb, sc[c]);
+      bool need = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m = mb;
+      } else if (mb > m + kLazyRescale) {
+        need = true;
+        alpha = ex2(m - mb);
+        m = mb;
+        l *= alpha;
+      }
+      if (__any_sync(kFull, need)) {
+        // O of the previous tile must be complete before it is rescaled
+        if (!wait_all(pfree + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) {
+          bad = true;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tc::ld32(tbase + lanes + 256 + 32 * half, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tc::st32(tbase + lanes + 256 + 32 * half, o);
+        }
+        tc::wait_st();
+      }
+      // P buffer s was last read by O of tile j - 2
+      if (j >= 2 && !wait_all(pfree + 8 * s, ((j >> 1) - 1) & 1)) {
+        bad = true;
+        break;
+      }
+      uint8_t* ph = sm + OFF_P + s * 2 * PPART;
+      uint8_t* pl = ph + PPART;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        sc[c] = ex2(sc[c] - m);
+        l += sc[c];
+      }
+#pragma unroll
+      for (int g = 0; g < BN / 8; ++g) {   // 16-byte chunks of 8 keys
+        uint32_t hi[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hi[e] = pack2<T>(sc[8 * g + 2 * e], sc[8 * g + 2 * e + 1]);
+        const uint32_t off = p_off(r, g);
+        *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        if (two_part) {
+          uint32_t lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 rh = unpack2<T>(hi[e]);
+            lo[e] = pack2<T>(sc[8 * g + 2 * e] - rh.x, sc[8 * g + 2 * e + 1] - rh.y);
+          }
+          *reinterpret_cast<uint4*>(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      // P (generic-proxy writes) goes to the tensor cores (async proxy)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull + 8 * s);
+    }
+    if (bad) {
+      if (lane == 0) fail();
+    } else if (wait_all(pfree + 8 * ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1)) {
+      tc::fence_after();
+      uint32_t o[2][32];
+      tc::ld32(tbase + lanes + 256, o[0]);
+      tc::ld32(tbase + lanes + 256 + 32, o[1]);
+      if (qi < a.seq_len) {
+        const float inv = 1.f / l;
+        const int64_t row = (static_cast<int64_t>(b) * a.seq_len + qi) * a.heads + h;
+        float4* dst = reinterpret_cast<float4*>(a.out + row * PD);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[8 * hh + i] = make_float4(__uint_as_float(o[hh][4 * i]) * inv,
+                                          __uint_as_float(o[hh][4 * i + 1]) * inv,
+                                          __uint_as_float(o[hh][4 * i + 2]) * inv,
+                                          __uint_as_float(o[hh][4 * i + 3]) * inv);
+        a.lse[row] = (m + log2f(l)) * 0.69314718055994530942f;
+      }
+    } else if (lane == 0) {
+      fail();
+    }
+  }
+
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after();
+    tc::dealloc(tbase, TCOLS);
+  }
+}
+
+}  // namespace
+}  // namespace pkvd
+
+extern "C" int prefill_d64_run(const pkvd_prefill_desc* desc, const void* q, const void* k,
+                               const void* v, float* out, float* lse, int32_t* status,
+                               pkvd_stream_t stream) {
+  using namespace pkvd;
+  if (!desc || !q || !k || !v || !out || !lse || !status) return PKVD_EINVAL;
+  const pkvd_prefill_desc& d = *desc;
+  if (d.batch < 1 || d.heads < 1 || d.kv_heads < 1 || d.seq_len < 1 || d.reserved[0] ||
+      d.reserved[1] || !(d.scale >= 0.f))
+    return PKVD_EINVAL;
+  if (d.dtype != PKVD_BF16 && d.dtype != PKVD_FP16) return PKVD_EINVAL;
+  if (d.heads % d.kv_heads != 0) return PKVD_EUNSUPPORTED;
+  for (const void* p : {q, k, v, static_cast<const void*>(out), static_cast<const void*>(lse)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return PKVD_EINVAL;
+  const int64_t q_tiles = (static_cast<int64_t>(d.seq_len) + BM - 1) / BM;
+  const int64_t blocks = q_tiles * d.batch * d.heads;
+  if (blocks > 0x7fffffffLL || static_cast<int64_t>(d.batch) * d.kv_heads > 0x7fffffffLL)
+    return PKVD_EUNSUPPORTED;
+
+  PrefillMaps maps;
+  const uint64_t L = static_cast<uint64_t>(d.seq_len);
+  {
+    const uint64_t dims[4] = {PD, static_cast<uint64_t>(d.heads), L, static_cast<uint64_t>(d.batch)};
+    const uint64_t strides[3] = {PD * 2, static_cast<uint64_t>(d.heads) * PD * 2,
+                                 L * d.heads * PD * 2};
+    const uint32_t box[4] = {PD, 1, BM, 1};
+    const int rc = encode_tiled_map(d.dtype, q, 4, dims, strides, box, &maps.q);
+    if (rc != PKVD_OK) return rc;
+  }
+  {
+    const uint64_t dims[3] = {PD, L, static_cast<uint64_t>(d.batch) * d.kv_heads};
+    const uint64_t strides[2] = {PD * 2, L * PD * 2};
+    const uint32_t box[3] = {PD, BN, 1};
+    int rc = encode_tiled_map(d.dtype, k, 3, dims, strides, box, &maps.k);
+    if (rc == PKVD_OK) rc = encode_tiled_map(d.dtype, v, 3, dims, strides, box, &maps.v);
+    if (rc != PKVD_OK) return rc;
+  }
+  PrefillArgs a;
+  a.out = out;
+  a.lse = lse;
+  a.status = status;
+  a.batch = d.batch;
+  a.heads = d.heads;
+  a.kv_heads = d.kv_heads;
+  a.seq_len = d.seq_len;
+  a.q_tiles = static_cast<int32_t>(q_tiles);
+  const float scale = d.scale > 0.f ? d.scale : 0.125f;   // 1 / sqrt(64)
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+
+  const void* fn = d.dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&prefill_d64<__half>)
+                                        : reinterpret_cast<const void*>(&prefill_d64<__nv_bfloat16>);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem) !=
+      cudaSuccess)
+    return PKVD_ECUDA;
+  void* args[] = {&a, &maps};
+  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args,
+                       static_cast<size_t>(kPrefillSmem),
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKVD_ECUDA;
+  return PKVD_OK;
+}

@@ -71,13 +71,6 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch, int slab_bytes) {
   return (ch >> 3) * slab_bytes + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
 
-// 2^x on the special-function unit (inputs here are <= 8 or -inf).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // One step of the transposing xor butterfly: lanes with `up` keep the upper
 // N values, the others the lower N, each combined with its partner's copy.
 template <int N, bool MAX>

@@ -254,6 +254,22 @@ def gqa_varlen(dtype: str = "bf16", seed: Optional[int] = None,
                     q_len=q_len)
 
 
+def prefill_case(*, batch: int, heads: int, kv_heads: int, seq_len: int, dtype: str = "bf16",
+                 seed: int = 0, name: Optional[str] = None) -> DecodeCase:
+    """Dense causal prefill at head_dim 64, as a case of the decode problem
+    with every token a query: q [B, L, Hq, 64] (q_len = L), K and V
+    [B, Hkv, L, 64] = one page of L tokens per request (page b of request b)."""
+    g = _gen(seed)
+    L = int(seq_len)
+    q = _randn((batch, L, heads, 64), g, dtype)
+    k = _randn((batch, kv_heads, L, 64), g, dtype)
+    v = _randn((batch, kv_heads, L, 64), g, dtype)
+    pt = torch.arange(batch, dtype=torch.int32).view(batch, 1)
+    return DecodeCase(name or f"prefill_d64_b{batch}_h{heads}kv{kv_heads}_L{L}", q, k, v, pt,
+                      torch.full((batch,), L, dtype=torch.int32), heads, kv_heads, 64, 64, L,
+                      64, 64, 0.125, dtype, False, 0, unique_rows=batch * L, q_len=L)
+
+
 def permute_pages(case: DecodeCase, seed: int) -> DecodeCase:
     """The same logical problem with every physical page relabelled: pages move
     to new pool slots and the page table follows them."""

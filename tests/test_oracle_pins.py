@@ -306,10 +306,29 @@ def pin_multi_token_library(mutation=0):
                     assert abs(lse[b, vh] - float(torch.logsumexp(s, 0))) < 1e-12
 
 
+def pin_prefill_as_decode(mutation=0):
+    # dense causal prefill = every token a query on one page per request:
+    # torch fp64 softmax with the upper triangle masked, per (request, head)
+    case = W.prefill_case(batch=2, heads=4, kv_heads=2, seq_len=23, seed=41)
+    out, lse = _decode(case, mutation)
+    q, k, v = case.q.double(), case.k_pages.double(), case.v_pages.double()
+    B, L, H, D = q.shape
+    g = H // case.kv_heads
+    mask = torch.triu(torch.ones(L, L, dtype=torch.bool), 1)
+    for b in range(B):
+        for h in range(H):
+            s = ((q[b, :, h] @ k[b, h // g].T) * case.scale).masked_fill(mask, -math.inf)
+            got_o = out[b].reshape(L, H, D)[:, h]
+            got_l = lse[b].reshape(L, H)[:, h]
+            np.testing.assert_allclose(got_o, (torch.softmax(s, -1) @ v[b, h // g]).numpy(),
+                                       rtol=0, atol=1e-12)
+            np.testing.assert_allclose(got_l, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
 PINS = [pin_decoders, pin_q_zero_mean, pin_single_key, pin_two_keys,
         pin_library_crosscheck, pin_head_groups, pin_relabelling, pin_split_merge,
         pin_merge_closed_form, pin_empty_request, pin_pairs_and_threads,
-        pin_multi_token_truncation, pin_multi_token_library]
+        pin_multi_token_truncation, pin_multi_token_library, pin_prefill_as_decode]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
