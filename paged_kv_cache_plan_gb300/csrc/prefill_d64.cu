@@ -18,7 +18,8 @@
 //     the rows near a sequence's start have a handful of keys, where one
 //     rounding of P alone would not average out), running sums in fp32;
 //   * warp 4: TMA producer (the query tile once, then K and V tiles of 128
-//     keys through two stages);
+//     keys through kStages stages: the next tiles' copies are in flight for
+//     several tiles' compute);
 //   * warp 5: tensor-memory allocation and the MMA issue: S = Q K^T
 //     (M = 128 queries, N = 128 keys, K = 64) into one of two S buffers, then
 //     O += P V (M = 128, N = 64, K = 128 keys) for both parts of P.
@@ -53,12 +54,14 @@ constexpr float kLazyRescale = 8.f;    // log2 units
 constexpr uint32_t TCOLS = 512;        // S buffers at columns 0 and 128, O at 256
 constexpr int kOnePartFrom = 1024;     // query positions from which P is one 16-bit part
 
-// shared memory: [Q][K0][K1][V0][V1][P0 hi][P0 lo][P1 hi][P1 lo][misc]
+// shared memory: [Q][K stages][V stages][P hi][P lo][misc]; one P tile (the
+// softmax writes P of tile j once O of tile j - 1 has read P of tile j - 1)
+constexpr int kStages = 4;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + TILE;
-constexpr int OFF_V = OFF_K + 2 * TILE;
-constexpr int OFF_P = OFF_V + 2 * TILE;
-constexpr int OFF_MISC = OFF_P + 4 * PPART;
+constexpr int OFF_V = OFF_K + kStages * TILE;
+constexpr int OFF_P = OFF_V + kStages * TILE;
+constexpr int OFF_MISC = OFF_P + 2 * PPART;
 constexpr int MISC = 256;
 constexpr int kPrefillSmem = 1024 + OFF_MISC + MISC;   // 1 KB alignment slack
 static_assert(kPrefillSmem <= 232448, "shared memory per block");
@@ -94,8 +97,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   uint8_t* misc = sm + OFF_MISC;
   const uint32_t bars = smem_addr(misc);
-  const uint32_t qfull = bars, kvfull = bars + 8, kvempty = bars + 24, sfull = bars + 40,
-                 sfree = bars + 56, pfull = bars + 72, pfree = bars + 88, drain = bars + 104;
+  const uint32_t qfull = bars, kvfull = bars + 8, kvempty = bars + 8 + 8 * kStages,
+                 sfull = bars + 8 + 16 * kStages, sfree = sfull + 16, pfull = sfree + 16,
+                 pfree = pfull + 8, drain = pfree + 8;
+  static_assert(8 + 16 * kStages + 16 + 16 + 8 + 8 + 8 <= 128, "barriers before the slot");
   uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 132);
 
@@ -117,14 +122,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&maps.k);
     tma_prefetch_desc(&maps.v);
     mbar_init(qfull, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(kvfull + 8 * i, 1);
       mbar_init(kvempty + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(sfull + 8 * i, 1);
       mbar_init(sfree + 8 * i, kSoftmaxWarps);
-      mbar_init(pfull + 8 * i, kSoftmaxWarps);
-      mbar_init(pfree + 8 * i, 1);
     }
+    mbar_init(pfull, kSoftmaxWarps);
+    mbar_init(pfree, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -147,8 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(smem_addr(sm + OFF_Q), &maps.q, 0, h, qt * BM, b, qfull);
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && (*abort_flag || !mbar_wait(kvempty + 8 * s, ((j >> 1) - 1) & 1))) {
+        const int s = j % kStages;
+        if (j >= kStages &&
+            (*abort_flag || !mbar_wait(kvempty + 8 * s, (j / kStages - 1) & 1))) {
           fail();
           break;
         }
@@ -159,8 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // copies still in flight must land before the block exits
       mbar_wait(qfull, 0);
-      for (int j = (issued >= 2 ? issued - 2 : 0); j < issued; ++j)
-        mbar_wait(kvfull + 8 * (j & 1), (j >> 1) & 1);
+      for (int j = (issued >= kStages ? issued - kStages : 0); j < issued; ++j)
+        mbar_wait(kvfull + 8 * (j % kStages), (j / kStages) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
@@ -173,15 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tO = tbase + 256;
       bool ok = mbar_wait(qfull, 0);
       auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (*abort_flag || !mbar_wait(kvfull + 8 * s, (j >> 1) & 1)) return false;
-        if (j >= 2 && (*abort_flag || !mbar_wait(sfree + 8 * s, ((j >> 1) - 1) & 1))) return false;
+        const int s = j % kStages, sb = j & 1;
+        if (*abort_flag || !mbar_wait(kvfull + 8 * s, (j / kStages) & 1)) return false;
+        if (j >= 2 && (*abort_flag || !mbar_wait(sfree + 8 * sb, ((j >> 1) - 1) & 1))) return false;
         tc::fence_after();
-        const uint32_t d = tbase + s * BN;
+        const uint32_t d = tbase + sb * BN;
         const uint64_t dk = dk0 + s * kTileStep;
 #pragma unroll
         for (int k = 0; k < PD / 16; ++k) tc::mma_f16(d, dq + 2 * k, dk + 2 * k, kIdS, k > 0);
-        tc::commit(sfull + 8 * s);
+        tc::commit(sfull + 8 * sb);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -190,14 +198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int s = j & 1;
-        if (*abort_flag || !mbar_wait(pfull + 8 * s, (j >> 1) & 1)) {
+        const int s = j % kStages;
+        if (*abort_flag || !mbar_wait(pfull, j & 1)) {
           ok = false;
           break;
         }
         tc::fence_after();
         const uint64_t dv = dv0 + s * kTileStep;
-        const uint64_t dph = dp0 + s * 2 * kPartStep, dpl = dph + kPartStep;
+        const uint64_t dph = dp0, dpl = dp0 + kPartStep;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           const uint64_t koff = (k >> 2) * kSlabStep + (k & 3) * 2;
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (two_part) tc::mma_f16(tO, dpl + koff, dv + k * (2048 >> 4), kIdO, true);
         }
         tc::commit(kvempty + 8 * s);
-        tc::commit(pfree + 8 * s);
+        tc::commit(pfree);
       }
       if (!ok) fail();
       // every product issued must be complete before the memory is freed
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(kFull, !*abort_flag && mbar_wait(bar, parity));
     };
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
+      const int s = j & 1;   // S buffer
       if (!wait_all(sfull + 8 * s, (j >> 1) & 1)) {
         bad = true;
         break;
@@ -250,9 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (j * BN + c > qi) sc[c] = -INFINITY;
       }
-      float mb = -INFINITY;
+      // block maximum as eight independent chains (a single chain of 128
+      // dependent maxima would cost its full latency every tile)
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mb = fmaxf(mb, sc[c]);
+      for (int k = 0; k < 8; ++k) mx[k] = sc[k];
+#pragma unroll
+      for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sc[c]);
+      const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       bool need = false;
       float alpha = 1.f;
       if (j == 0) {
@@ -263,12 +277,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mb;
         l *= alpha;
       }
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight chains again
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        sc[c] = ex2(sc[c] - m);
+        ls[c & 7] += sc[c];
+      }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      // O of tile j - 1 must be complete before its P tile is rewritten and
+      // before O is rescaled
+      if (j >= 1 && !wait_all(pfree, (j - 1) & 1)) {
+        bad = true;
+        break;
+      }
       if (__any_sync(kFull, need)) {
-        // O of the previous tile must be complete before it is rescaled
-        if (!wait_all(pfree + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) {
-          bad = true;
-          break;
-        }
         tc::fence_after();
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -280,18 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::wait_st();
       }
-      // P buffer s was last read by O of tile j - 2
-      if (j >= 2 && !wait_all(pfree + 8 * s, ((j >> 1) - 1) & 1)) {
-        bad = true;
-        break;
-      }
-      uint8_t* ph = sm + OFF_P + s * 2 * PPART;
+      uint8_t* ph = sm + OFF_P;
       uint8_t* pl = ph + PPART;
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        sc[c] = ex2(sc[c] - m);
-        l += sc[c];
-      }
 #pragma unroll
       for (int g = 0; g < BN / 8; ++g) {   // 16-byte chunks of 8 keys
         uint32_t hi[4];
@@ -312,11 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P (generic-proxy writes) goes to the tensor cores (async proxy)
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pfull + 8 * s);
+      if (lane == 0) mbar_arrive(pfull);
     }
     if (bad) {
       if (lane == 0) fail();
-    } else if (wait_all(pfree + 8 * ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1)) {
+    } else if (wait_all(pfree, (nkv - 1) & 1)) {
       tc::fence_after();
       uint32_t o[2][32];
       tc::ld32(tbase + lanes + 256, o[0]);
