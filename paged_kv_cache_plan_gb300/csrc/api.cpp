@@ -101,10 +101,23 @@ int launch(const pkvd_plan* p, const void* q, const void* k, const void* v,
                            pargs, static_cast<size_t>(p->s1p.smem), stream) != cudaSuccess)
         return PKVD_ECUDA;
     }
-    if (L.info.num_items > 0 &&
-        cudaLaunchKernel(p->s1.func, dim3(L.info.num_items), dim3(p->s1.threads), args,
-                         static_cast<size_t>(p->s1.smem), stream) != cudaSuccess)
-      return PKVD_ECUDA;
+    if (L.info.num_items > 0) {
+      // After shared-prefix items the per-request items need nothing they
+      // write: programmatic dependent launch lets them take the SMs the
+      // prefix grid's last blocks leave idle (they wait for the prefix grid
+      // only at their end, so the merge still follows both).
+      cudaLaunchConfig_t c1{};
+      c1.gridDim = dim3(static_cast<unsigned>(L.info.num_items));
+      c1.blockDim = dim3(static_cast<unsigned>(p->s1.threads));
+      c1.dynamicSmemBytes = static_cast<size_t>(p->s1.smem);
+      c1.stream = stream;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      at[0].val.programmaticStreamSerializationAllowed = 1;
+      c1.attrs = at;
+      c1.numAttrs = L.info.num_prefix_items > 0 ? 1 : 0;
+      if (cudaLaunchKernelExC(&c1, p->s1.func, args) != cudaSuccess) return PKVD_ECUDA;
+    }
   }
   if (ev_mid && cudaEventRecord(ev_mid, stream) != cudaSuccess) return PKVD_ECUDA;
 

@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
       // copies still in flight must land before the block exits
       for (int q = j; q < issued; ++q) mbar_wait(bars + 8 * (q % STAGES), (q / STAGES) & 1);
     }
+    pdl_wait_prerequisites();   // see the end of the kernel
     return;
   }
 
@@ -321,6 +322,12 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
       a.lse_part[(it.unit * HB + h) * a.lse_stride + it.partial_row] =
           empty ? -INFINITY : m_run[r] + log2f(l_run[r]);
   }
+  // Launched after shared-prefix items (programmatic dependent launch, so
+  // that these blocks fill SMs the prefix items leave): the block finishes
+  // only once the prefix grid has, so the merge, which waits on this grid,
+  // sees the prefix partials too. Without a prerequisite grid this returns
+  // at once.
+  pdl_wait_prerequisites();
 }
 
 }  // namespace

@@ -553,6 +553,11 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     tc::fence_after();
     tc::dealloc(tbase, TCOLS);
   }
+  // As the private-token kernel of a shared-prefix plan (programmatic
+  // dependent launch): finish only once the prefix grid has, so the merge,
+  // which waits on this grid, sees the prefix partials too. Without a
+  // prerequisite grid this returns at once.
+  pdl_wait_prerequisites();
 }
 
 }  // namespace

@@ -340,3 +340,27 @@ def _items_full(L, args, seq, **kw):
     assert rc == 0
     return [(w.request, w.unit, w.split, w.partial_row, w.tok_begin, w.tok_end, w.query_pos)
             for w in arr[:info.num_items]]
+
+
+def test_prefill_and_selftest_argument_errors(L):
+    # argument checks happen before any CUDA call, so they run here too
+    import ctypes
+    d = _lib.PrefillDesc()
+    d.batch, d.heads, d.kv_heads, d.seq_len, d.dtype = 1, 4, 2, 128, _lib.PKVD_BF16
+    buf = (ctypes.c_uint8 * 64)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    aligned = ctypes.c_void_p((p.value + 15) // 16 * 16)
+    ptrs = [aligned] * 6
+    assert L.prefill_d64_run(None, *ptrs, None) == _lib.PKVD_EINVAL
+    assert L.prefill_d64_run(ctypes.byref(d), None, *ptrs[1:], None) == _lib.PKVD_EINVAL
+    for field, bad in (("seq_len", 0), ("batch", 0), ("dtype", 7)):
+        e = _lib.PrefillDesc.from_buffer_copy(d)
+        setattr(e, field, bad)
+        assert L.prefill_d64_run(ctypes.byref(e), *ptrs, None) == _lib.PKVD_EINVAL
+    e = _lib.PrefillDesc.from_buffer_copy(d)
+    e.kv_heads = 3
+    assert L.prefill_d64_run(ctypes.byref(e), *ptrs, None) == _lib.PKVD_EUNSUPPORTED
+    misaligned = ctypes.c_void_p(aligned.value + 4)
+    assert L.prefill_d64_run(ctypes.byref(d), misaligned, *ptrs[1:], None) == _lib.PKVD_EINVAL
+    assert L.decode_selftest_wait_timeout(None, 1000, None) == _lib.PKVD_EINVAL
+    assert L.decode_selftest_wait_timeout(aligned, 0, None) == _lib.PKVD_EINVAL
