@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "device.cuh"
@@ -44,40 +45,58 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int PD = 64;                 // head dim (K and V)
 constexpr int BM = 128;                // queries per block
-constexpr int BN = 128;                // keys per tile
-constexpr int TILE = BN * PD * 2;      // 16 KB: a Q, K or V tile
+constexpr int TILE_Q = BM * PD * 2;    // 16 KB: the query tile
 constexpr int PSLAB = BM * 128;        // 16 KB: 128 rows x 64 keys of P
-constexpr int PPART = 2 * PSLAB;       // 32 KB: one part (high or low) of a P tile
 constexpr int kThreads = 192;
 constexpr int kSoftmaxWarps = 4, kProducerWarp = 4, kMmaWarp = 5;
 constexpr float kLazyRescale = 8.f;    // log2 units
-constexpr uint32_t TCOLS = 512;        // S buffers at columns 0 and 128, O at 256
 constexpr int kOnePartFrom = 1024;     // query positions from which P is one 16-bit part
-
-// shared memory: [Q][K stages][V stages][P hi][P lo][misc]; one P tile (the
-// softmax writes P of tile j once O of tile j - 1 has read P of tile j - 1)
-constexpr int kStages = 4;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;
-constexpr int OFF_V = OFF_K + kStages * TILE;
-constexpr int OFF_P = OFF_V + kStages * TILE;
-constexpr int OFF_MISC = OFF_P + 2 * PPART;
 constexpr int MISC = 256;
-constexpr int kPrefillSmem = 1024 + OFF_MISC + MISC;   // 1 KB alignment slack
-static_assert(kPrefillSmem <= 232448, "shared memory per block");
+
+// Two shapes of the kernel. Query tiles before kOnePartFrom tokens (rows
+// with few keys) keep P in two 16-bit parts and take 128-key tiles through
+// four stages (208 KB, one block per SM); the later ones use one part and
+// 64-key tiles (96 KB and 256 tensor-memory columns: two blocks per SM, so
+// that two blocks' softmax warps share each SM sub-partition).
+// Shared memory: [Q][K stages][V stages][P (high, low)][misc]; one P tile
+// (the softmax writes P of tile j once O of tile j - 1 has read P of j - 1).
+// Tensor memory: two S buffers of BN columns, then O (64 columns).
+template <int kBN, int kStages, bool kTwoPart, int kMinBlocks>
+struct PfShape {
+  static constexpr int BN = kBN;                 // keys per tile
+  static constexpr int STAGES = kStages;
+  static constexpr bool TWO = kTwoPart;
+  static constexpr int MINB = kMinBlocks;        // resident blocks per SM
+  static constexpr int TILE_KV = BN * PD * 2;    // a K or V tile
+  static constexpr int PPART = BM * BN * 2;      // one part of P
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE_Q;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_KV;
+  static constexpr int OFF_P = OFF_V + STAGES * TILE_KV;
+  static constexpr int OFF_MISC = OFF_P + (TWO ? 2 : 1) * PPART;
+  static constexpr int SMEM = 1024 + OFF_MISC + MISC;   // 1 KB alignment slack
+  static constexpr uint32_t OCOL = 2 * BN;               // O after the two S buffers
+  static constexpr uint32_t TCOLS = OCOL + PD <= 256 ? 256 : 512;
+  static_assert(SMEM * MINB + 1024 * MINB <= 233472, "shared memory per SM");
+  static_assert(TCOLS * MINB <= 512, "tensor memory per SM");
+  static_assert(BM % BN == 0 && BN % 64 == 0, "key tiles of 64 or 128");
+};
+using EarlyShape = PfShape<128, 4, true, 1>;
+using LateShape = PfShape<64, 4, false, 2>;
 
 struct PrefillArgs {
   float* out;            // [B, L, Hq, 64]
   float* lse;            // [B, L, Hq] natural log
   int32_t* status;       // device status word (kStatus* bits)
   int32_t batch, heads, kv_heads, seq_len;
-  int32_t q_tiles;       // ceil(L / 128)
+  int32_t qt_first;      // query tiles qt_first .. qt_first + qt_count - 1
+  int32_t qt_count;
   float scale_log2;
 };
 
 struct PrefillMaps {
   CUtensorMap q;         // {64, Hq, L, B}, box {64, 1, 128, 1}
-  CUtensorMap k;         // {64, L, B * Hkv}, box {64, 128, 1}
+  CUtensorMap k;         // {64, L, B * Hkv}, box {64, BN, 1}
   CUtensorMap v;
 };
 
@@ -86,16 +105,20 @@ __device__ __forceinline__ uint32_t p_off(int r, int c) {
   return (c >> 3) * PSLAB + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 7) ^ (r & 7))) << 4);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, typename C>
+__global__ void __launch_bounds__(kThreads, C::MINB)
     prefill_d64(const __grid_constant__ PrefillArgs a, const __grid_constant__ PrefillMaps maps) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  constexpr int BN = C::BN, kStages = C::STAGES, TILE = C::TILE_KV, PPART = C::PPART;
+  constexpr int OFF_Q = C::OFF_Q, OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_P = C::OFF_P;
+  constexpr bool two_part = C::TWO;
+  constexpr uint32_t TCOLS = C::TCOLS;
   constexpr uint32_t kIdS = tc::idesc_f16(kBf16, BM, BN, false, false);
   constexpr uint32_t kIdO = tc::idesc_f16(kBf16, BM, PD, false, true);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  uint8_t* misc = sm + OFF_MISC;
+  uint8_t* misc = sm + C::OFF_MISC;
   const uint32_t bars = smem_addr(misc);
   const uint32_t qfull = bars, kvfull = bars + 8, kvempty = bars + 8 + 8 * kStages,
                  sfull = bars + 8 + 16 * kStages, sfree = sfull + 16, pfull = sfree + 16,
@@ -107,16 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // heavy (late) query tiles first
   const int bh_count = a.batch * a.heads;
-  const int qt = a.q_tiles - 1 - static_cast<int>(blockIdx.x) / bh_count;
+  const int qt = a.qt_first + a.qt_count - 1 - static_cast<int>(blockIdx.x) / bh_count;
   const int bh = static_cast<int>(blockIdx.x) % bh_count;
   const int b = bh / a.heads, h = bh % a.heads;
   const int kvh = h / (a.heads / a.kv_heads);
-  const int nkv = qt + 1;                      // key tiles 0 .. qt
-  // P in two 16-bit parts while some row of the tile has few keys (the rows
-  // of tiles at or past kOnePartFrom tokens see more than that many keys,
-  // where the rounding of a one-part P averages out)
-  const bool two_part = qt * BM < kOnePartFrom;
+  constexpr int kPer = BM / BN;                // key tiles per query tile
+  const int nkv = (qt + 1) * kPer;             // key tiles up to the diagonal
+  const int jdiag = qt * kPer;                 // first key tile that needs the causal mask
 
+  pdl_launch_dependents();   // the second launch may take SMs this grid's tail leaves
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&maps.q);
     tma_prefetch_desc(&maps.k);
@@ -150,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA
     if (lane == 0) {
       const int kvrow = b * a.kv_heads + kvh;
-      mbar_arrive_expect_tx(qfull, TILE);
+      mbar_arrive_expect_tx(qfull, TILE_Q);
       tma_load_4d(smem_addr(sm + OFF_Q), &maps.q, 0, h, qt * BM, b, qfull);
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
@@ -178,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv0 = tc::sdesc(smem_addr(sm + OFF_V), TILE, 1024);       // MN-major
       const uint64_t dp0 = tc::sdesc(smem_addr(sm + OFF_P), 16, 1024);         // K-major
       constexpr uint64_t kTileStep = TILE >> 4, kPartStep = PPART >> 4, kSlabStep = PSLAB >> 4;
-      const uint32_t tO = tbase + 256;
+      const uint32_t tO = tbase + C::OCOL;
       bool ok = mbar_wait(qfull, 0);
       auto issue_s = [&](int j) -> bool {
         const int s = j % kStages, sb = j & 1;
@@ -243,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ts = tbase + lanes + s * BN;
       float sc[BN];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c4 = 0; c4 < BN / 32; ++c4) {
         uint32_t x[32];
         tc::ld32(ts + 32 * c4, x);
 #pragma unroll
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sfree + 8 * s);
-      if (j == qt) {
+      if (j >= jdiag) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (j * BN + c > qi) sc[c] = -INFINITY;
@@ -295,10 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t o[32];
-          tc::ld32(tbase + lanes + 256 + 32 * half, o);
+          tc::ld32(tbase + lanes + C::OCOL + 32 * half, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tc::st32(tbase + lanes + 256 + 32 * half, o);
+          tc::st32(tbase + lanes + C::OCOL + 32 * half, o);
         }
         tc::wait_st();
       }
@@ -331,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (wait_all(pfree, (nkv - 1) & 1)) {
       tc::fence_after();
       uint32_t o[2][32];
-      tc::ld32(tbase + lanes + 256, o[0]);
-      tc::ld32(tbase + lanes + 256 + 32, o[1]);
+      tc::ld32(tbase + lanes + C::OCOL, o[0]);
+      tc::ld32(tbase + lanes + C::OCOL + 32, o[1]);
       if (qi < a.seq_len) {
         const float inv = 1.f / l;
         const int64_t row = (static_cast<int64_t>(b) * a.seq_len + qi) * a.heads + h;
@@ -358,6 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     tc::dealloc(tbase, TCOLS);
   }
+  // The second launch (programmatic dependent launch) finishes only once the
+  // first has, so whatever follows in the stream sees both; for the first
+  // launch this returns at once.
+  pdl_wait_prerequisites();
 }
 
 }  // namespace
@@ -381,24 +407,6 @@ extern "C" int prefill_d64_run(const pkvd_prefill_desc* desc, const void* q, con
   if (blocks > 0x7fffffffLL || static_cast<int64_t>(d.batch) * d.kv_heads > 0x7fffffffLL)
     return PKVD_EUNSUPPORTED;
 
-  PrefillMaps maps;
-  const uint64_t L = static_cast<uint64_t>(d.seq_len);
-  {
-    const uint64_t dims[4] = {PD, static_cast<uint64_t>(d.heads), L, static_cast<uint64_t>(d.batch)};
-    const uint64_t strides[3] = {PD * 2, static_cast<uint64_t>(d.heads) * PD * 2,
-                                 L * d.heads * PD * 2};
-    const uint32_t box[4] = {PD, 1, BM, 1};
-    const int rc = encode_tiled_map(d.dtype, q, 4, dims, strides, box, &maps.q);
-    if (rc != PKVD_OK) return rc;
-  }
-  {
-    const uint64_t dims[3] = {PD, L, static_cast<uint64_t>(d.batch) * d.kv_heads};
-    const uint64_t strides[2] = {PD * 2, L * PD * 2};
-    const uint32_t box[3] = {PD, BN, 1};
-    int rc = encode_tiled_map(d.dtype, k, 3, dims, strides, box, &maps.k);
-    if (rc == PKVD_OK) rc = encode_tiled_map(d.dtype, v, 3, dims, strides, box, &maps.v);
-    if (rc != PKVD_OK) return rc;
-  }
   PrefillArgs a;
   a.out = out;
   a.lse = lse;
@@ -407,19 +415,55 @@ extern "C" int prefill_d64_run(const pkvd_prefill_desc* desc, const void* q, con
   a.heads = d.heads;
   a.kv_heads = d.kv_heads;
   a.seq_len = d.seq_len;
-  a.q_tiles = static_cast<int32_t>(q_tiles);
   const float scale = d.scale > 0.f ? d.scale : 0.125f;   // 1 / sqrt(64)
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
 
-  const void* fn = d.dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&prefill_d64<__half>)
-                                        : reinterpret_cast<const void*>(&prefill_d64<__nv_bfloat16>);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem) !=
-      cudaSuccess)
-    return PKVD_ECUDA;
-  void* args[] = {&a, &maps};
-  if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), args,
-                       static_cast<size_t>(kPrefillSmem),
-                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKVD_ECUDA;
-  return PKVD_OK;
+  const uint64_t L = static_cast<uint64_t>(d.seq_len);
+  PrefillMaps maps;
+  {
+    const uint64_t dims[4] = {PD, static_cast<uint64_t>(d.heads), L, static_cast<uint64_t>(d.batch)};
+    const uint64_t strides[3] = {PD * 2, static_cast<uint64_t>(d.heads) * PD * 2,
+                                 L * d.heads * PD * 2};
+    const uint32_t box[4] = {PD, 1, BM, 1};
+    const int rc = encode_tiled_map(d.dtype, q, 4, dims, strides, box, &maps.q);
+    if (rc != PKVD_OK) return rc;
+  }
+  // one launch per kernel shape: query tiles before kOnePartFrom tokens, then the rest
+  const int64_t early = std::min<int64_t>(q_tiles, kOnePartFrom / BM);
+  bool after_first = false;   // the second launch overlaps the first's tail
+  auto launch = [&](auto shape, int64_t qt_first, int64_t qt_count) -> int {
+    using C = decltype(shape);
+    if (qt_count <= 0) return PKVD_OK;
+    const uint64_t dims[3] = {PD, L, static_cast<uint64_t>(d.batch) * d.kv_heads};
+    const uint64_t strides[2] = {PD * 2, L * PD * 2};
+    const uint32_t box[3] = {PD, C::BN, 1};
+    int rc = encode_tiled_map(d.dtype, k, 3, dims, strides, box, &maps.k);
+    if (rc == PKVD_OK) rc = encode_tiled_map(d.dtype, v, 3, dims, strides, box, &maps.v);
+    if (rc != PKVD_OK) return rc;
+    a.qt_first = static_cast<int32_t>(qt_first);
+    a.qt_count = static_cast<int32_t>(qt_count);
+    const void* fn = d.dtype == PKVD_FP16 ? reinterpret_cast<const void*>(&prefill_d64<__half, C>)
+                                          : reinterpret_cast<const void*>(&prefill_d64<__nv_bfloat16, C>);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return PKVD_ECUDA;
+    void* args[] = {&a, &maps};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(qt_count * d.batch * d.heads));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(C::SMEM);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = after_first ? 1 : 0;
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return PKVD_ECUDA;
+    after_first = true;
+    return PKVD_OK;
+  };
+  // the long late tiles first, so the short early ones fill the tail
+  int rc = launch(LateShape{}, early, q_tiles - early);
+  if (rc == PKVD_OK) rc = launch(EarlyShape{}, 0, early);
+  return rc;
 }
