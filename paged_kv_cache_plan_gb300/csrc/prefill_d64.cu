@@ -61,8 +61,9 @@ constexpr int MISC = 256;
 // Shared memory: [Q][K stages][V stages][P (high, low)][misc]; one P tile
 // (the softmax writes P of tile j once O of tile j - 1 has read P of j - 1).
 // Tensor memory: two S buffers of BN columns, then O (64 columns).
-template <int kBN, int kStages, bool kTwoPart, int kMinBlocks>
+template <int kBN, int kStages, bool kTwoPart, int kMinBlocks, int kSBuf>
 struct PfShape {
+  static constexpr int SBUF = kSBuf;             // S buffers in tensor memory
   static constexpr int BN = kBN;                 // keys per tile
   static constexpr int STAGES = kStages;
   static constexpr bool TWO = kTwoPart;
@@ -75,14 +76,14 @@ struct PfShape {
   static constexpr int OFF_P = OFF_V + STAGES * TILE_KV;
   static constexpr int OFF_MISC = OFF_P + (TWO ? 2 : 1) * PPART;
   static constexpr int SMEM = 1024 + OFF_MISC + MISC;   // 1 KB alignment slack
-  static constexpr uint32_t OCOL = 2 * BN;               // O after the two S buffers
-  static constexpr uint32_t TCOLS = OCOL + PD <= 256 ? 256 : 512;
+  static constexpr uint32_t OCOL = SBUF * BN;            // O after the S buffers
+  static constexpr uint32_t TCOLS = OCOL + PD <= 128 ? 128 : OCOL + PD <= 256 ? 256 : 512;
   static_assert(SMEM * MINB + 1024 * MINB <= 233472, "shared memory per SM");
   static_assert(TCOLS * MINB <= 512, "tensor memory per SM");
   static_assert(BM % BN == 0 && BN % 64 == 0, "key tiles of 64 or 128");
 };
-using EarlyShape = PfShape<128, 4, true, 1>;
-using LateShape = PfShape<64, 4, false, 2>;
+using EarlyShape = PfShape<128, 4, true, 1, 2>;
+using LateShape = PfShape<64, 2, false, 3, 1>;
 
 struct PrefillArgs {
   float* out;            // [B, L, Hq, 64]
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
       mbar_init(kvfull + 8 * i, 1);
       mbar_init(kvempty + 8 * i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::SBUF; ++i) {
       mbar_init(sfull + 8 * i, 1);
       mbar_init(sfree + 8 * i, kSoftmaxWarps);
     }
@@ -203,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
       const uint32_t tO = tbase + C::OCOL;
       bool ok = mbar_wait(qfull, 0);
       auto issue_s = [&](int j) -> bool {
-        const int s = j % kStages, sb = j & 1;
+        const int s = j % kStages, sb = j % C::SBUF;
         if (*abort_flag || !mbar_wait(kvfull + 8 * s, (j / kStages) & 1)) return false;
-        if (j >= 2 && (*abort_flag || !mbar_wait(sfree + 8 * sb, ((j >> 1) - 1) & 1))) return false;
+        if (j >= C::SBUF &&
+            (*abort_flag || !mbar_wait(sfree + 8 * sb, (j / C::SBUF - 1) & 1)))
+          return false;
         tc::fence_after();
         const uint32_t d = tbase + sb * BN;
         const uint64_t dk = dk0 + s * kTileStep;
@@ -254,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
       return __all_sync(kFull, !*abort_flag && mbar_wait(bar, parity));
     };
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;   // S buffer
-      if (!wait_all(sfull + 8 * s, (j >> 1) & 1)) {
+      const int s = j % C::SBUF;   // S buffer
+      if (!wait_all(sfull + 8 * s, (j / C::SBUF) & 1)) {
         bad = true;
         break;
       }
