@@ -104,14 +104,6 @@ __device__ __forceinline__ void issue_block(const Stage1Args& a, const KvTensorM
   }
 }
 
-// Warm L2 with block blk's K and V tiles (TILES only; lanes 0 and 1).
-template <int D, bool TILES>
-__device__ __forceinline__ void prefetch_block(const KvTensorMaps& maps, int64_t row, int lane) {
-  if constexpr (TILES) {
-    if (lane < 2) tma_prefetch_l2_3d(lane ? &maps.v : &maps.k, 0, static_cast<int32_t>(row), 0);
-  }
-}
-
 // Pool rows of a warp's first blocks: the SPW blocks it copies first and
 // the PF blocks after them (the page-id window). Loaded at the very start of
 // the block, before the barrier set-up, so that the page-table round trip
@@ -139,10 +131,10 @@ struct WarpRows {
 // The per-warp pipeline: issue this warp's first SPW blocks, then for each of
 // its blocks wait, run `process(nv, stage, k0)` (nv valid rows, k0 = the
 // block's first token relative to the item), and refill the stage with the
-// block SPW further on. With TILES, the blocks PFL beyond the next refill are
-// also prefetched into L2 (off: it did not pay). Returns false when a wait ran
-// out (after waiting, bounded, for this warp's copies still in flight). The
-// caller's `prologue` runs once the first copies are in flight.
+// block SPW further on (prefetching further blocks into L2 was measured and
+// did not pay). Returns false when a wait ran out (after waiting, bounded,
+// for this warp's copies still in flight). The caller's `prologue` runs once
+// the first copies are in flight.
 template <int D, bool TILES, typename P, typename F>
 __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTensorMaps& maps,
                                               const pkvd_work_item& it, WarpRows<D, TILES>& wr,
@@ -152,8 +144,6 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
   constexpr int SPW = gqa_stages_per_warp(D);
   constexpr int SB = gqa_stage_bytes(D, TILES);
   constexpr int PF = WarpRows<D, TILES>::PF;
-  constexpr int PFL = 0;              // L2 prefetch distance past the next refill (off)
-  static_assert(PFL < PF, "prefetched rows come from the page-id window");
   const int n = it.tok_end - it.tok_begin;
   const int nblk = (n + BLK - 1) / BLK;
   const int nmine = nblk > warp ? (nblk - warp + W - 1) / W : 0;
@@ -168,9 +158,6 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
   for (int s = 0; s < SPW; ++s)
     if (s < nmine)
       issue_block<D, TILES>(a, maps, blk_of(s), n, wr.first[s], stage_of(s), bar_of(s), lane);
-#pragma unroll
-  for (int i = 0; i < PFL; ++i)
-    if (SPW + i < nmine) prefetch_block<D, TILES>(maps, rows[i], lane);
   prologue();
 
   bool ok = true;
@@ -188,8 +175,6 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
           if (k + SPW < nmine)
             issue_block<D, TILES>(a, maps, blk_of(k + SPW), n, rows[i], stage_of(k), bar_of(k),
                                   lane);
-          if (PFL > 0 && k + SPW + PFL < nmine)
-            prefetch_block<D, TILES>(maps, rows[(i + PFL) % PF], lane);
           rows[i] = kv_row_of(a, it, pt, blk_of(k + SPW + PF), nblk, r);
           ++k;
         }
