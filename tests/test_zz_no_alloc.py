@@ -35,6 +35,11 @@ CASES = {
                               seq_lens=[5000, 17, 900], pool_pages=500, seed=301),
     "mla": lambda: W.mla_case(batch=2, heads=16, seq_len=3000, prefix_len=2000, group=2,
                               pool_rows=9000, seed=302),
+    # several query tokens per request
+    "gqa_q3": lambda: W.gqa_case(batch=2, heads=8, kv_heads=2, head_dim=128, page_size=16,
+                                 seq_lens=[700, 33], pool_pages=60, seed=303, q_len=3),
+    "mla_q4": lambda: W.mla_case(batch=2, heads=16, seq_len=2000, prefix_len=0,
+                                 pool_rows=5000, seed=304, q_len=4),
 }
 
 
@@ -45,11 +50,12 @@ def test_static_scratch_matches_planned_entry_point(cuda_ok, name):
     plan = plan_for_case(case)
     ref_out, ref_lse = run_case(plan, dev)
     torch.cuda.synchronize()
-    ref_out, ref_lse = ref_out.cpu().double().numpy(), ref_lse.cpu().double().numpy()
+    vh = case.q_len * case.heads   # (query token, head) rows per request
+    ref_out = ref_out.reshape(case.batch, vh, case.head_dim_v).cpu().double().numpy()
+    ref_lse = ref_lse.reshape(case.batch, vh).cpu().double().numpy()
     for call in range(2):
-        out = torch.full_like(dev.q.new_empty((case.batch, case.heads, case.head_dim_v),
-                                              dtype=torch.float32), float("nan"))
-        lse = torch.full((case.batch, case.heads), float("nan"), device="cuda")
+        out = torch.full((case.batch, vh, case.head_dim_v), float("nan"), device="cuda")
+        lse = torch.full((case.batch, vh), float("nan"), device="cuda")
         _lib.check(_run_static(plan.desc, case, dev, out, lse), "decode_run_static")
         torch.cuda.synchronize()
         o = out.cpu().double().numpy()
