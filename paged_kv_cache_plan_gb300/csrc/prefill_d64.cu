@@ -12,23 +12,27 @@
 //
 // One block per (request, query head, 128-query tile); six warps:
 //   * warps 0-3: softmax, one query row per thread (tensor-memory lane =
-//     row); scores are read from tensor memory twice (block maximum, then P),
-//     P = exp2(s - m) goes to shared memory as a 16-bit high part plus the
-//     16-bit rounding of its remainder (two products, ~16 significant bits:
-//     the rows near a sequence's start have a handful of keys, where one
-//     rounding of P alone would not average out), running sums in fp32;
-//   * warp 4: TMA producer (the query tile once, then K and V tiles of 128
-//     keys through kStages stages: the next tiles' copies are in flight for
-//     several tiles' compute);
+//     row); the row's scores of a key tile are read from tensor memory once
+//     into registers, masked on the diagonal tiles, P = exp2(s - m) goes to
+//     shared memory, running sums in fp32;
+//   * warp 4: TMA producer (the query tile once, then K and V tiles through
+//     several stages, so the next tiles' copies are in flight during the
+//     current tile's compute);
 //   * warp 5: tensor-memory allocation and the MMA issue: S = Q K^T
-//     (M = 128 queries, N = 128 keys, K = 64) into one of two S buffers, then
-//     O += P V (M = 128, N = 64, K = 128 keys) for both parts of P.
-// The running maximum is lazy (raised only when a block's maximum exceeds it
-// by more than 2^8); a raise rescales the thread's O row in tensor memory
-// after the previous O product is complete. Causality: key tiles 0 .. qt of
-// query tile qt; the diagonal tile masks keys after the row's own position.
-// Every wait is bounded; a wait that runs out sets the status word, and every
-// role drains what it issued before the block frees its tensor memory.
+//     (M = 128 queries, N = the tile's keys, K = 64) into an S buffer, then
+//     O += P V (M = 128, N = 64, K = the tile's keys).
+// Two shapes (PfShape below): query tiles before kOnePartFrom tokens keep P
+// as a 16-bit high part plus the 16-bit rounding of its remainder (two
+// products, ~16 significant bits: their first rows have a handful of keys,
+// where one rounding of P would not average out) with 128-key tiles, one
+// block per SM; later tiles use one part and 64-key tiles, small enough for
+// three blocks per SM. The running maximum is lazy (raised only when a
+// block's maximum exceeds it by more than 2^8); a raise rescales the
+// thread's O row in tensor memory after the previous O product is complete.
+// Causality: key tiles up to the diagonal of query tile qt; the diagonal
+// tiles mask keys after the row's own position. Every wait is bounded; a
+// wait that runs out sets the status word, and every role drains what it
+// issued before the block frees its tensor memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
