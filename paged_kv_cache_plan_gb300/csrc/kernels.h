@@ -77,7 +77,8 @@ bool mla_tc_kernel(int dtype, bool causal, KernelEntry* e);
 // The merge kernel of a plan (threads and shared memory filled in): one
 // thread per column when no request has more than kMergeColMaxSplits
 // splits; otherwise split-parallel, with deep prefetch when the merge grid
-// (batch x heads x Dv slices blocks) is at most two blocks per SM.
+// (batch x rows x Dv slices blocks, rows = q_len x heads) is at most two
+// blocks per SM.
 bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, KernelEntry* e);
 
 // Stage-1 kernel for a normalised plan description (variant resolved).

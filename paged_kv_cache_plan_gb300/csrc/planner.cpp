@@ -15,7 +15,7 @@
 // sharing); it is a pure relabelling, so results are bit-identical.
 //
 // Merge tiling (the same page, Technical Details 3): slice Dv only while
-// the B * Hq merge blocks would leave SMs idle, up to 8 ways, and only into
+// the B * q_len * Hq merge blocks would leave SMs idle, up to 8 ways, and only into
 // slices that divide Dv evenly.
 #include "planner.h"
 

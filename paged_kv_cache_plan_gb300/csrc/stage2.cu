@@ -1,4 +1,6 @@
-// Stage 2: merge the split partials of every (request, head).
+// Stage 2: merge the split partials of every (request, query token, head)
+// row (one query token: every (request, head)); `heads` below counts these
+// rows per request.
 //
 // For request b with S splits (partial rows r0 .. r0 + S - 1), head h:
 //     M = max_s lse_s,  w_s = 2^(lse_s - M)          (log2 domain)
@@ -6,7 +8,7 @@
 // Splits of an empty range carry lse = -inf and weight 0; no split at all
 // (an empty request) gives out = 0 and lse = -inf.
 //
-// Grid: (B * Hq, tiles). With tiles > 1 each block owns a disjoint slice of
+// Grid: (B * rows, tiles). With tiles > 1 each block owns a disjoint slice of
 // the Dv output columns and re-derives M and sum_s w_s on its own, so the
 // slices never communicate -- the head-dim-tiled stage-2 reduce of the
 // aiter pull 4758 page (Technical Details 3). The merge waits on stage 1
