@@ -3,6 +3,11 @@
     plan = decode_plan(batch, heads, kv_heads, head_dim, page_size, seq_lens, splits)
     decode_run(plan, q, k_pages, v_pages, page_table, out, lse)
 
+Several query tokens per request (make_desc(..., q_len=n), n > 1): q, out and
+lse carry a token axis, [B, n, Hq, ...], and token j sees the cache up to its
+own position L - n + j. prefill_d64(q, k, v) runs the dense causal prefill at
+head_dim 64. decode_plan_prefix plans MLA requests that share a prefix.
+
 Tensors are torch CUDA tensors (PyTorch provides device memory and streams
 only). Shapes, dtypes and alignment are checked here; the arithmetic runs in
 the library's kernels.
