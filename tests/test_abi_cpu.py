@@ -364,3 +364,10 @@ def test_prefill_and_selftest_argument_errors(L):
     assert L.prefill_d64_run(ctypes.byref(d), misaligned, *ptrs[1:], None) == _lib.PKVD_EINVAL
     assert L.decode_selftest_wait_timeout(None, 1000, None) == _lib.PKVD_EINVAL
     assert L.decode_selftest_wait_timeout(aligned, 0, None) == _lib.PKVD_EINVAL
+
+
+def test_query_token_plans_cover_every_token_once(L):
+    for args, seq, q in (((3, 8, 2, 128, 16), [300, 5, 4099], 3),
+                         ((2, 16, 1, 576, 1), [2000, 70], 4)):
+        info, items = _plan(*args, seq=seq, q_len=q)
+        _check_cover(info, items, seq, info["units_per_request"])

@@ -306,6 +306,32 @@ def pin_multi_token_library(mutation=0):
                     assert abs(lse[b, vh] - float(torch.logsumexp(s, 0))) < 1e-12
 
 
+def pin_multi_token_split_merge(mutation=0):
+    # split partials of a query token's row, merged, equal its one-shot
+    # result; a split past the token's own position is empty (lse -inf)
+    case = _multi_token_cases()[0]
+    out, lse = _decode(case, mutation)
+    P = _P(case, mutation)
+    H = case.heads
+    for b in range(case.batch):
+        L = int(case.seq_lens[b])
+        for j in range(case.q_len):
+            vh = j * H + (b % H)
+            cuts = sorted({max(1, L // 3), max(1, L - 2), L})
+            parts, lses, t0 = [], [], 0
+            for t1 in cuts:
+                o, l = oracle.partial(P, case.q, case.k_pages, case.v_pages, case.page_table,
+                                      case.seq_lens, b, vh, t0, t1)
+                if t0 > L - case.q_len + j:   # nothing here is visible to token j
+                    assert l == -math.inf and np.all(o == 0)
+                parts.append(o)
+                lses.append(l)
+                t0 = t1
+            mo, ml = oracle.merge(np.stack(parts), np.array(lses), mutation)
+            np.testing.assert_allclose(mo, out[b, vh], rtol=0, atol=1e-12)
+            assert abs(ml - lse[b, vh]) < 1e-12
+
+
 def pin_prefill_as_decode(mutation=0):
     # dense causal prefill = every token a query on one page per request:
     # torch fp64 softmax with the upper triangle masked, per (request, head)
@@ -328,7 +354,8 @@ def pin_prefill_as_decode(mutation=0):
 PINS = [pin_decoders, pin_q_zero_mean, pin_single_key, pin_two_keys,
         pin_library_crosscheck, pin_head_groups, pin_relabelling, pin_split_merge,
         pin_merge_closed_form, pin_empty_request, pin_pairs_and_threads,
-        pin_multi_token_truncation, pin_multi_token_library, pin_prefill_as_decode]
+        pin_multi_token_truncation, pin_multi_token_library, pin_multi_token_split_merge,
+        pin_prefill_as_decode]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
