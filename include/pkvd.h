@@ -28,8 +28,8 @@
  *     Motivation and Technical Details.
  *
  * Two families:
- *   GQA  head_dim D in {128, 256}, head_dim_v == D, heads / kv_heads in
- *        {1, 2, 4, 8, 16}; K and V in separate pools.
+ *   GQA  head_dim D in {128, 256}, head_dim_v == D, heads / kv_heads from 1
+ *        to 16 (the FMA variant: 1, 2, 4 or 8); K and V in separate pools.
  *   MLA  head_dim 576 (512 no-rope + 64 rope), head_dim_v 512, kv_heads 1,
  *        heads a multiple of 16; V is the first 512 elements of the same
  *        576-wide row (pass v_pages == k_pages, both row pitches equal).

@@ -1,9 +1,11 @@
 """ctypes binding of the C ABI in include/pkvd.h (argument marshalling only).
 
-The names match the C entry points: decode_plan, decode_plan_ex, decode_run,
-decode_run_timed, decode_plan_destroy, decode_workspace_bytes,
-decode_plan_query, decode_last_device_status, decode_plan_compute,
-decode_status_string. Every step of the computation runs in libpkvd.so's
+The names match the C entry points: decode_plan, decode_plan_ex,
+decode_plan_prefix, decode_run, decode_run_timed, decode_run_static,
+decode_plan_destroy, decode_workspace_bytes, decode_plan_query,
+decode_last_device_status, decode_plan_compute, decode_plan_prefix_compute,
+decode_status_string, decode_selftest_wait_timeout, prefill_d64_run. Every
+step of the computation runs in libpkvd.so's
 CUDA kernels; if the library is missing this module raises instead of
 falling back to anything else.
 """
