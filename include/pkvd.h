@@ -52,9 +52,10 @@
  *
  * Errors. Every call returns a pkvd_status (0 = success) and never aborts.
  * decode_run is asynchronous: it reports argument and launch errors only.
- * Faults the kernels detect themselves (a page id outside the pool when
- * checks are on, a pipeline wait that ran out) are recorded in a device
- * status word and come back from decode_last_device_status.
+ * Faults the kernels detect themselves (with checks on: a page id outside
+ * the pool, or members of a shared-prefix group whose prefix pages differ;
+ * always: a pipeline wait that ran out) are recorded in a device status word
+ * and come back from decode_last_device_status.
  *
  * Streams. decode_run enqueues work on the given stream and neither
  * allocates nor synchronises, so it can be captured in a CUDA graph.
@@ -79,7 +80,7 @@ typedef enum pkvd_status {
   PKVD_EUNSUPPORTED = -2,   /* valid but unsupported shape or dtype         */
   PKVD_ECUDA = -3,          /* a CUDA runtime call failed                   */
   PKVD_ENOMEM = -4,         /* host or device allocation failed             */
-  PKVD_EDEVICE_CHECK = -5,  /* a kernel found a page id outside the pool    */
+  PKVD_EDEVICE_CHECK = -5,  /* a kernel's page-id check failed (checks on)  */
   PKVD_ETIMEOUT = -6        /* a kernel's bounded pipeline wait ran out     */
 } pkvd_status;
 
@@ -95,8 +96,10 @@ typedef enum pkvd_variant {
   PKVD_VARIANT_MLA_MMA = 3,   /* mma.sync, a block of 16 heads per work item       */
   PKVD_VARIANT_MLA_TC = 4     /* tcgen05 with tensor-memory accumulators, a block
                                  of 64 heads per work item (heads % 64 == 0); P
-                                 is rounded to one 16-bit value, so AUTO takes it
-                                 only when every request has >= 1024 tokens     */
+                                 is rounded to one 16-bit value, so it is taken
+                                 (AUTO) and accepted (forced) only when every
+                                 non-empty request has >= 1024 tokens; else
+                                 PKVD_EUNSUPPORTED                              */
 } pkvd_variant;
 
 /* Order of stage-1 work items in the grid. Both orders compute the same
@@ -186,13 +189,21 @@ typedef struct pkvd_work_item {
 
 /* GQA shorthand of decode_plan_ex (head_dim_v = head_dim, bf16, all other
  * fields default); head_dim 576 selects the MLA family (Dv 512, pitches 576).
- * seq_lens: host array of `batch` lengths, copied. splits: 0 = planner. */
+ * seq_lens: host array of `batch` lengths, copied. splits: 0 = planner.
+ * Defined by: aiter pull 4758, Motivation (the split count per request, about
+ * 256 / batch on that part, trades loop length against parallelism). */
 int decode_plan(pkvd_plan **out, int batch, int heads, int kv_heads, int head_dim,
                 int page_size, const int32_t *seq_lens, int splits);
 
 /* Make a plan on the current CUDA device: checks the shape, runs the split
  * planner, allocates and fills the device work list and the partial
- * workspace. *out receives the plan (NULL on error). */
+ * workspace. *out receives the plan (NULL on error). PKVD_EINVAL for a bad
+ * field, PKVD_EUNSUPPORTED for a shape no kernel takes, PKVD_ENOMEM /
+ * PKVD_ECUDA if the device allocation or upload failed.
+ * Defined by: aiter pull 4758, Motivation (split count) and Technical
+ * Details 2 (split-major grid order) and 3 (head-dim-tiled merge gated on
+ * idle SMs); ROCm/rocm-libraries pull 10102, Motivation (a launch must be
+ * keyed by every shape field: a plan is valid only for its own). */
 int decode_plan_ex(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens);
 
 /* Shared-prefix plan (MLA only, heads in {16, 32, 64}). prefix_group[b] >= 0
@@ -200,27 +211,43 @@ int decode_plan_ex(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *s
  * requests with equal prefix_len[b] (1 <= prefix_len[b] <= seq_lens[b]) and
  * page_table rows whose first ceil(prefix_len / page_size) entries name the
  * same pages (the caller's promise: the shared tokens are read through the
- * first member's row). prefix_group[b] < 0: no sharing. The
+ * first member's row; with desc->checks on, the kernels compare every
+ * member's prefix entries with the first member's and report a difference
+ * as PKVD_EDEVICE_CHECK). prefix_group[b] < 0: no sharing. A group's
  * shared tokens are read once per 64/heads members, with the members' query
  * heads batched as the N side of the tensor-core products (64 rows); each
- * request's private tokens run as usual, and the merge combines both kinds
- * of partials. This is the aiter pull 4758 page's hope of L2 reuse under
- * prefix sharing (Technical Details 2) made explicit. Results equal the
- * plain plan's within the usual tolerance. desc->splits applies to the
- * private tokens only. */
+ * request's private tokens run as usual (their variant is chosen on the
+ * private lengths), and the merge combines both kinds of partials. Groups
+ * whose prefix is shorter than 1024 tokens are not batched (their members
+ * read the prefix as private tokens): the batched items run on the
+ * tensor-memory kernel, whose one-part P needs long items. Results equal
+ * the plain plan's within the usual tolerance. desc->splits applies to the
+ * private tokens only.
+ * Defined by: aiter pull 4758, Technical Details 2 (the split-major grid
+ * hopes for L2 reuse when requests share a prefix; this call makes the
+ * reuse explicit) and Test Plan (68,000-token contexts whose first 63,240
+ * tokens are shared by groups of 8). */
 int decode_plan_prefix(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens,
                        const int32_t *prefix_group, const int32_t *prefix_len);
 
 /* Host-only planning of a shared-prefix plan (no CUDA call): the grouped
  * prefix items come first in `items`, then the per-request items; capacity
  * must cover info->num_prefix_items + info->num_items. desc->num_sms and
- * desc->ctas_per_sm (of the per-request kernel) must be set. */
+ * desc->ctas_per_sm (of the per-request kernel) must be set.
+ * Defined by: as decode_plan_prefix. */
 int decode_plan_prefix_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
                                const int32_t *prefix_group, const int32_t *prefix_len,
                                pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
 
 /* Launch stage 1 and the merge on `stream`. q, k_pages, v_pages, page_table,
- * out and lse are device pointers laid out as above. Asynchronous. */
+ * out and lse are device pointers laid out as above. Asynchronous; returns
+ * PKVD_EINVAL for a null or misaligned pointer or a plan made on another
+ * device, PKVD_ECUDA if a launch failed.
+ * Defined by: aiter pull 4758, Motivation (stage 1 writes one normalised
+ * partial and its log-sum-exp per split; stage 2 merges them) and Technical
+ * Details 1 (two KV blocks in flight in the stage-1 loop) and 3 (the merge
+ * recomputes its scalar statistics per Dv tile); TensorFold pull 1932, "What
+ * this changes" (one score per key for each query head of a KV group). */
 int decode_run(const pkvd_plan *plan, const void *q, const void *k_pages,
                const void *v_pages, const int32_t *page_table, float *out, float *lse,
                pkvd_stream_t stream);
@@ -228,24 +255,37 @@ int decode_run(const pkvd_plan *plan, const void *q, const void *k_pages,
 /* decode_run that also records caller-made events on `stream`: ev_begin
  * before stage 1, ev_mid between stage 1 and the merge, ev_end after the
  * merge (any may be NULL). Recording ev_mid keeps the merge from overlapping
- * stage 1's tail; otherwise identical to decode_run. For timing each stage. */
+ * stage 1's tail; otherwise identical to decode_run. For timing each stage.
+ * Defined by: aiter pull 4758, Test Plan (device time from events around
+ * the op) and Technical Details 3 (stage-2's own share is measured). */
 int decode_run_timed(const pkvd_plan *plan, const void *q, const void *k_pages,
                      const void *v_pages, const int32_t *page_table, float *out,
                      float *lse, pkvd_stream_t stream, pkvd_event_t ev_begin,
                      pkvd_event_t ev_mid, pkvd_event_t ev_end);
 
 /* Free a plan and its device memory (NULL is a no-op). Synchronises the
- * plan's device so no run still reads the freed memory. */
+ * plan's device so no run still reads the freed memory. PKVD_ECUDA if the
+ * synchronisation or the free failed (the plan is freed on the host anyway).
+ * Defined by: the plan / run split of decode_plan_ex (ROCm/rocm-libraries
+ * pull 10102, Motivation). */
 int decode_plan_destroy(pkvd_plan *plan);
 
-/* Device bytes the plan owns (work list, split table, partials, status). */
+/* Device bytes the plan owns (work list, split table, partials, status); 0
+ * for NULL. Defined by: aiter pull 4758, Motivation (the per-split partials
+ * and their log-sum-exps that stage 1 leaves for the merge). */
 size_t decode_workspace_bytes(const pkvd_plan *plan);
 
-/* Copy the planner's decisions into *info. */
+/* Copy the planner's decisions into *info (PKVD_EINVAL for NULL).
+ * Defined by: aiter pull 4758, Motivation and Technical Details 2-3 (split
+ * count, grid order and merge tiling are the planner's decisions). */
 int decode_plan_query(const pkvd_plan *plan, pkvd_plan_info *info);
 
 /* Synchronise `stream`, then read and clear the plan's device status word:
- * PKVD_OK, PKVD_EDEVICE_CHECK or PKVD_ETIMEOUT. */
+ * PKVD_OK, PKVD_EDEVICE_CHECK or PKVD_ETIMEOUT (PKVD_ECUDA if the
+ * synchronisation or the read failed).
+ * Defined by: TensorFold pull 1932, "What this changes" and "Tests run" (a
+ * key or block the kernel skips must be caught, not pass silently): here
+ * every pipeline wait is bounded and reports, and page ids can be checked. */
 int decode_last_device_status(const pkvd_plan *plan, pkvd_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -303,7 +343,10 @@ int decode_selftest_wait_timeout(int32_t *status, int64_t limit_us, pkvd_stream_
  * desc->ctas_per_sm must be set (> 0). Fills *info and, when `items` is not
  * NULL, up to `capacity` work items in grid order. Returns PKVD_OK, or
  * PKVD_EINVAL when capacity is smaller than info->num_items (info is still
- * filled). */
+ * filled).
+ * Defined by: aiter pull 4758, Motivation (split count) and Technical
+ * Details 2 (split-major order); ROCm/rocm-libraries pull 10102, Technical
+ * Details (the structure is checked on the host, without a GPU). */
 int decode_plan_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
                         pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
 
@@ -321,15 +364,28 @@ int decode_plan_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens,
  *   - All calls share the array: calls on one stream run in order, calls that
  *     overlap on the GPU (other streams, unsynchronised threads) race.
  *   - The first call on a device looks up the array's address with that
- *     device current; make it before any stream capture.
- *   - Device-side page-id checks and wait timeouts are not reported.
+ *     device current.
+ *   - The call copies its work list from host memory it frees on return, so
+ *     on a stream that is being captured it returns PKVD_EUNSUPPORTED and
+ *     queues nothing.
+ *   - Device-side page-id checks (desc->checks) and wait timeouts are
+ *     recorded in the array's status word, which each call clears first;
+ *     decode_run_static_status reports the last call's.
  * q, k_pages, v_pages, page_table, out and lse are as for decode_run;
  * desc and seq_lens are host pointers, read during the call only. */
 int decode_run_static(const pkvd_plan_desc *desc, const int32_t *seq_lens, const void *q,
                       const void *k_pages, const void *v_pages, const int32_t *page_table,
                       float *out, float *lse, pkvd_stream_t stream);
 
-/* Static description of a status code. */
+/* Status of the last decode_run_static call on the current device, also
+ * allocation-free (the paper has no counterpart to this call either):
+ * synchronises `stream`, then reads and clears the static array's status
+ * word. PKVD_OK, PKVD_EDEVICE_CHECK (a page id outside the pool, with
+ * checks on) or PKVD_ETIMEOUT (a pipeline wait ran out). */
+int decode_run_static_status(pkvd_stream_t stream);
+
+/* Static description of a status code (never NULL). Defined by: the
+ * error conventions above. */
 const char *decode_status_string(int status);
 
 #ifdef __cplusplus

@@ -93,10 +93,9 @@ def lib() -> ctypes.CDLL:
             L.orc_decode_threads.argtypes = [P, vp, vp, vp, vp, vp, i32, vp, vp]
             L.orc_partial.argtypes = [P, vp, vp, vp, vp, vp, i32, i32, i64, i64, vp, vp]
             L.orc_merge.argtypes = [i32, i32, vp, vp, i32, vp, vp]
-            L.orc_scores.argtypes = [P, vp, vp, vp, vp, i32, i32, vp]
             L.orc_to_double.argtypes = [vp, i64, i32, vp]
             for f in ("orc_decode", "orc_decode_pairs", "orc_decode_threads",
-                      "orc_partial", "orc_merge", "orc_scores"):
+                      "orc_partial", "orc_merge"):
                 getattr(L, f).restype = ctypes.c_int
             L.orc_to_double.restype = None
             _lib = L
@@ -168,18 +167,6 @@ def decode(P: Problem, q, k_pages, v_pages, page_table, seq_lens, *,
                             _ptr(v_pages), _ptr(pt), _ptr(sl), _ptr(out),
                             _ptr(lse)), "decode")
     return out, lse
-
-
-def scores(P: Problem, q, k_pages, page_table, seq_lens, b: int, h: int):
-    """Scaled fp64 scores of (b, v) (v = token * Hq + head) for all of the
-    request's tokens in logical order (no causal cut)."""
-    L = lib()
-    pt, sl = _i32(page_table), _i32(seq_lens)
-    n = int(np.asarray(sl)[b]) if not hasattr(sl, "data_ptr") else int(sl[b])
-    s = np.zeros((max(n, 1),), dtype=np.float64)
-    _check(L.orc_scores(ctypes.byref(P), _ptr(q), _ptr(k_pages), _ptr(pt),
-                        _ptr(sl), int(b), int(h), _ptr(s)), "scores")
-    return s[:n]
 
 
 def partial(P: Problem, q, k_pages, v_pages, page_table, seq_lens, b, h, t0, t1):

@@ -215,17 +215,6 @@ static int check_problem(const orc_problem *P) {
   return 0;
 }
 
-/* Scaled scores of (b, v) for all of the request's tokens: s[0 .. L_b)
- * (no causal cut: the caller reads the ones it needs). */
-int orc_scores(const orc_problem *P, const uint16_t *q, const uint16_t *k,
-               const int32_t *page_table, const int32_t *seq_lens, int32_t b,
-               int32_t h, double *s) {
-  int rc = check_problem(P);
-  if (rc) return rc;
-  scores(P, q, k, page_table, seq_lens, b, h, 0, seq_lens[b], s);
-  return 0;
-}
-
 /* Full decode for every (b, v): out [B, q_len * Hq, Dv] (= [B, q_len, Hq,
  * Dv]), lse [B, q_len * Hq]. */
 int orc_decode(const orc_problem *P, const uint16_t *q, const uint16_t *k,

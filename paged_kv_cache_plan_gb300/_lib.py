@@ -2,7 +2,7 @@
 
 The names match the C entry points: decode_plan, decode_plan_ex,
 decode_plan_prefix, decode_run, decode_run_timed, decode_run_static,
-decode_plan_destroy, decode_workspace_bytes, decode_plan_query,
+decode_run_static_status, decode_plan_destroy, decode_workspace_bytes, decode_plan_query,
 decode_last_device_status, decode_plan_compute, decode_plan_prefix_compute,
 decode_status_string, decode_selftest_wait_timeout, prefill_d64_run. Every
 step of the computation runs in libpkvd.so's
@@ -85,6 +85,7 @@ SIGNATURES = {
                                                   ctypes.POINTER(PlanInfo), _vp, _i64]),
     "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
+    "decode_run_static_status": (ctypes.c_int, [_vp]),
     "decode_selftest_wait_timeout": (ctypes.c_int, [_vp, _i64, _vp]),
     "prefill_d64_run": (ctypes.c_int, [ctypes.POINTER(PrefillDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp]),

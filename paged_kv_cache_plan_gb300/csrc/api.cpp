@@ -180,14 +180,18 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
               const int32_t* prefix_group, const int32_t* prefix_len) {
   if (!out || !desc) return PKVD_EINVAL;
   *out = nullptr;
+  const bool prefix = prefix_group != nullptr;
+  // the per-request items' description (a shared-prefix plan resolves their
+  // variant on the private lengths)
   pkvd_plan_desc d;
   int family = 0;
-  int rc = pkvd::normalise_desc(*desc, seq_lens, &d, &family);
+  int rc = prefix ? pkvd::prefix_private_desc(*desc, seq_lens, prefix_group, prefix_len, &d,
+                                              &family)
+                  : pkvd::normalise_desc(*desc, seq_lens, &d, &family);
   if (rc != PKVD_OK) return rc;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
-  const bool prefix = prefix_group != nullptr;
   pkvd::KernelEntry s1, s1p, s2;
   if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, seq_lens), &s1))
     return PKVD_EUNSUPPORTED;
@@ -398,7 +402,7 @@ const char* decode_status_string(int status) {
     case PKVD_EUNSUPPORTED: return "unsupported shape or dtype";
     case PKVD_ECUDA: return "CUDA runtime error";
     case PKVD_ENOMEM: return "out of memory";
-    case PKVD_EDEVICE_CHECK: return "a kernel found a page id outside the pool";
+    case PKVD_EDEVICE_CHECK: return "a kernel page-id check failed (an id outside the pool, or shared-prefix pages that differ)";
     case PKVD_ETIMEOUT: return "a kernel pipeline wait timed out";
     default: return "unknown status";
   }

@@ -16,7 +16,8 @@ namespace pkvd {
 
 // Bits of the device status word.
 constexpr int kStatusTimeout = 1;   // a pipeline wait ran out
-constexpr int kStatusBadPage = 2;   // a page id outside [0, num_pool_pages)
+constexpr int kStatusBadPage = 2;   // a page id outside [0, num_pool_pages), or (grouped
+                                    // shared-prefix items) members whose prefix pages differ
 
 // A pipeline wait gives up after this long (the kernel then records
 // kStatusTimeout, drains its own copies and returns).

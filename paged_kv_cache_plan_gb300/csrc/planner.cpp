@@ -127,18 +127,22 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
   const int group = d.heads / d.kv_heads;
   const int vheads = d.q_len * d.heads;
   if (mla) {
-    if (d.variant == PKVD_VARIANT_AUTO) {
-      // tensor-memory kernel for 64-row blocks over long contexts, where
-      // its one-part P rounding averages out (see kMlaTcMinContext)
-      int64_t min_len = INT64_MAX;
-      for (int b = 0; b < d.batch; ++b) min_len = std::min<int64_t>(min_len, seq_lens[b]);
-      d.variant = vheads % kMlaTcHeads == 0 && min_len >= kMlaTcMinContext
-                      ? PKVD_VARIANT_MLA_TC
-                      : PKVD_VARIANT_MLA_MMA;
-    }
+    // The tensor-memory kernel rounds P to one 16-bit value; it is only
+    // taken (and only accepted) when every non-empty request has at least
+    // kMlaTcMinContext tokens, where that rounding averages out far below
+    // the output tolerance. Shorter contexts run on the mma.sync kernel,
+    // which keeps a second, low part of P.
+    int64_t min_len = INT64_MAX;
+    for (int b = 0; b < d.batch; ++b)
+      if (seq_lens[b] > 0) min_len = std::min<int64_t>(min_len, seq_lens[b]);
+    const bool long_enough = min_len >= kMlaTcMinContext;
+    if (d.variant == PKVD_VARIANT_AUTO)
+      d.variant = vheads % kMlaTcHeads == 0 && long_enough ? PKVD_VARIANT_MLA_TC
+                                                           : PKVD_VARIANT_MLA_MMA;
     if (d.variant != PKVD_VARIANT_MLA_MMA && d.variant != PKVD_VARIANT_MLA_TC)
       return PKVD_EUNSUPPORTED;
-    if (d.variant == PKVD_VARIANT_MLA_TC && vheads % kMlaTcHeads != 0) return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_MLA_TC && (vheads % kMlaTcHeads != 0 || !long_enough))
+      return PKVD_EUNSUPPORTED;
   } else {
     // The mma consumer is faster than the fp32 FMA consumer on every group
     // size measured on GB300 (the FMA path is issue-bound: about five
@@ -313,50 +317,93 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   return PKVD_OK;
 }
 
-int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
-                       const int32_t* prefix_group, const int32_t* prefix_len,
-                       PlanLayout* out) {
+namespace {
+
+struct Group {
+  int first, count;
+  int64_t len;
+};
+
+// Checks the sharing description and collects the groups that get grouped
+// prefix items: runs of consecutive requests with one group id and one
+// prefix length. A group whose prefix is shorter than kMlaTcMinContext is
+// dropped (its members read the prefix as private tokens): the grouped
+// items run on the tensor-memory kernel, whose one-part P needs long items.
+// plen[b] = the shared tokens request b skips in its private items.
+int prefix_groups(const pkvd_plan_desc& in, const int32_t* seq_lens,
+                  const int32_t* prefix_group, const int32_t* prefix_len,
+                  std::vector<Group>* groups, std::vector<int32_t>* plen) {
   if (!prefix_group || !prefix_len || !seq_lens || in.batch < 1) return PKVD_EINVAL;
   const int B = in.batch;
   if (in.head_dim != kMlaDk) return PKVD_EUNSUPPORTED;
-  // normalise on the full lengths (page-table width, variant), then plan the
-  // private tokens with that description
-  pkvd_plan_desc nd;
-  int family = 0;
-  int nrc = normalise_desc(in, seq_lens, &nd, &family);
-  if (nrc != PKVD_OK) return nrc;
-  if (nd.q_len != 1) return PKVD_EUNSUPPORTED;   // one query token per shared-prefix request
   if (in.heads < 1 || kMlaTcHeads % in.heads != 0 || in.heads % kMlaHeads != 0)
     return PKVD_EUNSUPPORTED;
-  const int per_unit = kMlaTcHeads / in.heads;   // requests whose heads fill 64 rows
-
-  // groups: runs of consecutive requests with one group id and prefix length
-  struct Group {
-    int first, count;
-    int64_t len;
-  };
-  std::vector<Group> groups;
-  std::vector<int32_t> plen(B, 0);
+  groups->clear();
+  plen->assign(B, 0);
+  std::vector<int> ids;   // group id of every group seen, kept or dropped
   for (int b = 0; b < B; ++b) {
     if (seq_lens[b] < 0) return PKVD_EINVAL;
     const int g = prefix_group[b];
     if (g < 0) continue;
     if (prefix_len[b] < 1 || prefix_len[b] > seq_lens[b]) return PKVD_EINVAL;
-    plen[b] = prefix_len[b];
     if (b > 0 && prefix_group[b - 1] == g) {
       if (prefix_len[b] != prefix_len[b - 1]) return PKVD_EINVAL;
-      ++groups.back().count;
+      if (!groups->empty() && groups->back().first + groups->back().count == b &&
+          prefix_group[groups->back().first] == g)
+        ++groups->back().count;
     } else {
-      for (const Group& o : groups)
-        if (prefix_group[o.first] == g) return PKVD_EINVAL;   // members not consecutive
-      groups.push_back({b, 1, prefix_len[b]});
+      for (int o : ids)
+        if (o == g) return PKVD_EINVAL;   // members not consecutive
+      ids.push_back(g);
+      if (prefix_len[b] >= kMlaTcMinContext) groups->push_back({b, 1, prefix_len[b]});
     }
   }
+  for (const Group& g : *groups)
+    for (int m = 0; m < g.count; ++m) (*plen)[g.first + m] = static_cast<int32_t>(g.len);
+  return PKVD_OK;
+}
+
+}  // namespace
+
+int prefix_private_desc(const pkvd_plan_desc& in, const int32_t* seq_lens,
+                        const int32_t* prefix_group, const int32_t* prefix_len,
+                        pkvd_plan_desc* out, int* family) {
+  std::vector<Group> groups;
+  std::vector<int32_t> plen;
+  int rc = prefix_groups(in, seq_lens, prefix_group, prefix_len, &groups, &plen);
+  if (rc != PKVD_OK) return rc;
+  // normalise on the full lengths (page-table width, scale, pitches), then
+  // resolve the variant again on the private lengths
+  pkvd_plan_desc nd;
+  rc = normalise_desc(in, seq_lens, &nd, family);
+  if (rc != PKVD_OK) return rc;
+  if (nd.q_len != 1) return PKVD_EUNSUPPORTED;   // one query token per shared-prefix request
+  nd.variant = in.variant;
+  std::vector<int32_t> rest(in.batch);
+  for (int b = 0; b < in.batch; ++b) rest[b] = seq_lens[b] - plen[b];
+  return normalise_desc(nd, rest.data(), out, family);
+}
+
+int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
+                       const int32_t* prefix_group, const int32_t* prefix_len,
+                       PlanLayout* out) {
+  std::vector<Group> groups;
+  std::vector<int32_t> plen;
+  int rc = prefix_groups(in, seq_lens, prefix_group, prefix_len, &groups, &plen);
+  if (rc != PKVD_OK) return rc;
+  const int B = in.batch;
+  const int per_unit = kMlaTcHeads / in.heads;   // requests whose heads fill 64 rows
+  pkvd_plan_desc nd;
+  int family = 0;
+  rc = prefix_private_desc(in, seq_lens, prefix_group, prefix_len, &nd, &family);
+  if (rc != PKVD_OK) return rc;
+  nd.num_sms = in.num_sms;
+  nd.ctas_per_sm = in.ctas_per_sm;
 
   // the private tokens: an ordinary plan on the suffix lengths
   std::vector<int32_t> rest(B);
   for (int b = 0; b < B; ++b) rest[b] = seq_lens[b] - plen[b];
-  int rc = plan_layout(nd, rest.data(), out);
+  rc = plan_layout(nd, rest.data(), out);
   if (rc != PKVD_OK) return rc;
   PlanLayout& P = *out;
   P.seq_lens.assign(seq_lens, seq_lens + B);
@@ -376,7 +423,10 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
   if (!groups.empty()) {
     int64_t best = -1;
     for (int64_t S = 1; S <= 256; ++S) {
-      const int64_t c = std::max<int64_t>(2 * blk, ceil_div(ceil_div(maxp, S), blk) * blk);
+      // no prefix split shorter than kMlaTcMinContext (only a prefix's last
+      // split can be, and its weight in the merge is small)
+      const int64_t c = std::max<int64_t>(ceil_div(kMlaTcMinContext, blk) * blk,
+                                          ceil_div(ceil_div(maxp, S), blk) * blk);
       const int64_t cost = ceil_div(items_for(c), target) * (c + 2 * blk);
       if (best < 0 || cost < best) {
         best = cost;

@@ -42,6 +42,13 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
 // Full planning with desc->num_sms and desc->ctas_per_sm already set (> 0).
 int plan_layout(const pkvd_plan_desc& desc, const int32_t* seq_lens, PlanLayout* out);
 
+// The normalised description of a shared-prefix plan's per-request items:
+// the full lengths fix the page-table width, the private lengths (what is
+// left after the grouped prefixes) resolve the variant.
+int prefix_private_desc(const pkvd_plan_desc& in, const int32_t* seq_lens,
+                        const int32_t* prefix_group, const int32_t* prefix_len,
+                        pkvd_plan_desc* out, int* family);
+
 // Shared-prefix planning (see decode_plan_prefix): the per-request items of
 // the private tokens, planned as plan_layout does, plus grouped prefix items
 // for the tensor-memory MLA kernel (one resident block per SM).

@@ -216,9 +216,15 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       if (tok >= it.tok_end) tok = it.tok_end - 1;
       const int pidx = tok / a.page_size;
       int page = __ldg(pt + pidx);
-      if (a.checks && (page < 0 || page >= a.num_pool_pages)) {
-        atomicOr(a.status, kStatusBadPage);
-        page = 0;
+      if (a.checks) {
+        // a grouped item reads the shared tokens through its first member's
+        // page table: the other members must name the same pages
+        for (int m = 1; it.grouped && m < it.unit; ++m)
+          if (__ldg(pt + m * a.pt_stride + pidx) != page) atomicOr(a.status, kStatusBadPage);
+        if (page < 0 || page >= a.num_pool_pages) {
+          atomicOr(a.status, kStatusBadPage);
+          page = 0;
+        }
       }
       return (static_cast<int64_t>(page) * a.page_size + (tok - pidx * a.page_size)) *
              pitch_bytes;

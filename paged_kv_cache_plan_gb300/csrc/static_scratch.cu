@@ -18,9 +18,14 @@
 //     overlap on the GPU (different streams, or different host threads
 //     without ordering) race on it;
 //   * the first call on a device looks up the array's device address (with
-//     that device current); make that first call before any stream capture;
-//   * device-side checks and timeouts are recorded in the array's status
-//     word (cleared at the start of each call) but not reported back.
+//     that device current);
+//   * the work list and split table are copied from host memory that the
+//     call owns only while it runs, so the call refuses a stream that is
+//     being captured (PKVD_EUNSUPPORTED, nothing queued);
+//   * device-side page-id checks and wait timeouts are recorded in the
+//     array's status word, cleared at the start of each call;
+//     decode_run_static_status reads the last call's word (allocating
+//     nothing) and reports it like decode_last_device_status.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -71,6 +76,9 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
                                  pkvd_stream_t stream_handle) {
   if (!desc || !out || !lse) return PKVD_EINVAL;
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capturing) != cudaSuccess) return PKVD_ECUDA;
+  if (capturing != cudaStreamCaptureStatusNone) return PKVD_EUNSUPPORTED;
 
   pkvd_plan_desc d;
   int family = 0;
@@ -154,6 +162,7 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
     a.v = v_pages;
     a.page_table = page_table;
     a.items = d_items;
+    a.split_base = d_split;
     a.o_part = d_opart;
     a.lse_part = d_lpart;
     a.lse_stride = L.info.num_partial_rows;
@@ -205,5 +214,21 @@ extern "C" int decode_run_static(const pkvd_plan_desc* desc, const int32_t* seq_
   cfg.attrs = attr;
   cfg.numAttrs = any_work ? 1 : 0;
   if (cudaLaunchKernelExC(&cfg, s2.func, margs) != cudaSuccess) return PKVD_ECUDA;
+  return PKVD_OK;
+}
+
+extern "C" int decode_run_static_status(pkvd_stream_t stream_handle) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
+  unsigned char* base = nullptr;
+  int rc = scratch_address(dev, &base);
+  if (rc != PKVD_OK) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_handle)) != cudaSuccess)
+    return PKVD_ECUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, base, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PKVD_ECUDA;
+  if (v != 0 && cudaMemset(base, 0, sizeof(v)) != cudaSuccess) return PKVD_ECUDA;
+  if (v & 1) return PKVD_ETIMEOUT;
+  if (v & 2) return PKVD_EDEVICE_CHECK;
   return PKVD_OK;
 }

@@ -102,25 +102,37 @@ def _gen(seed: int) -> torch.Generator:
 
 
 def _randn(shape, g: torch.Generator, dtype: str, chunk_rows: int = 1 << 16) -> torch.Tensor:
-    """N(0,1) fp32 rounded to ``dtype``; drawn in row chunks to bound memory."""
+    """N(0,1) fp32 rounded to ``dtype``, on g's device; drawn in row chunks to
+    bound memory."""
     shape = tuple(int(s) for s in shape)
-    out = torch.empty(shape, dtype=_DT[dtype])
+    out = torch.empty(shape, dtype=_DT[dtype], device=g.device)
     flat = out.view(shape[0], -1)
     for r0 in range(0, shape[0], chunk_rows):
         r1 = min(shape[0], r0 + chunk_rows)
         flat[r0:r1] = torch.randn((r1 - r0, flat.shape[1]), generator=g,
-                                  dtype=torch.float32).to(_DT[dtype])
+                                  dtype=torch.float32, device=g.device).to(_DT[dtype])
     return out
+
+
+def _value_gen(seed: int, g: torch.Generator, device: str) -> torch.Generator:
+    """Generator of the values: the structure generator itself on the CPU;
+    on another device a generator there, seeded from the same seed (same
+    distribution and structure, other draws: for timing only)."""
+    if str(device) == "cpu":
+        return g
+    gd = torch.Generator(device=device)
+    gd.manual_seed(int(seed) + 0x5EED)
+    return gd
 
 
 def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
              page_size: int, seq_lens: Sequence[int], pool_pages: Optional[int] = None,
              dtype: str = "bf16", seed: int = 0, splits: int = 0,
              scale: Optional[float] = None, name: str = "gqa",
-             q_len: int = 1) -> DecodeCase:
+             q_len: int = 1, device: str = "cpu") -> DecodeCase:
     """GQA decode: Hq query heads over Hkv KV heads (consecutive groups),
     HND pages [P, Hkv, ps, D], a seeded random page scatter; q_len query
-    tokens per request."""
+    tokens per request. device != "cpu" draws the values there (timing only)."""
     lens = [int(x) for x in seq_lens]
     assert len(lens) == batch
     g = _gen(seed)
@@ -128,10 +140,11 @@ def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
     need = sum(npages)
     P = need if pool_pages is None else int(pool_pages)
     assert P >= need, "pool too small for the requested contexts"
+    gv = _value_gen(seed, g, device)
     q = _randn((batch, heads, head_dim) if q_len == 1 else (batch, q_len, heads, head_dim),
-               g, dtype)
-    k = _randn((max(P, 1), kv_heads, page_size, head_dim), g, dtype)
-    v = _randn((max(P, 1), kv_heads, page_size, head_dim), g, dtype)
+               gv, dtype)
+    k = _randn((max(P, 1), kv_heads, page_size, head_dim), gv, dtype)
+    v = _randn((max(P, 1), kv_heads, page_size, head_dim), gv, dtype)
     perm = torch.randperm(max(P, 1), generator=g).to(torch.int32)
     maxp = max(1, max(npages) if npages else 1)
     pt = torch.zeros((batch, maxp), dtype=torch.int32)
@@ -139,7 +152,8 @@ def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
     for b, n in enumerate(npages):
         pt[b, :n] = perm[nxt:nxt + n]
         nxt += n
-    return DecodeCase(name, q, k, v, pt, torch.tensor(lens, dtype=torch.int32), heads,
+    return DecodeCase(name, q, k, v, pt.to(q.device),
+                      torch.tensor(lens, dtype=torch.int32, device=q.device), heads,
                       kv_heads, head_dim, head_dim, page_size, head_dim, head_dim,
                       float(scale if scale is not None else 1.0 / math.sqrt(head_dim)),
                       dtype, False, splits, unique_rows=sum(lens), q_len=q_len)
@@ -148,19 +162,21 @@ def gqa_case(*, batch: int = 1, heads: int, kv_heads: int, head_dim: int,
 def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
              group: int = 8, pool_rows: Optional[int] = None, dtype: str = "bf16",
              seed: int = 0, splits: int = 0, scale: Optional[float] = None,
-             name: str = "mla", q_len: int = 1) -> DecodeCase:
+             name: str = "mla", q_len: int = 1, device: str = "cpu") -> DecodeCase:
     """MLA decode: one 576-wide latent row (512 + 64) per token shared by all
     heads, page size 1. Requests in consecutive groups of ``group`` share the
     physical rows of their first ``prefix_len`` tokens; the rest are private.
     Rows are scattered over the pool by a seeded permutation; only the rows a
-    request reads are drawn (the rest of the pool stays zero)."""
+    request reads are drawn (the rest of the pool stays zero). device !=
+    "cpu" draws the values there (timing only)."""
     D, DV = 576, 512
     g = _gen(seed)
     ngroups = (batch + group - 1) // group if prefix_len > 0 else 0
     unique = ngroups * prefix_len + batch * (seq_len - prefix_len)
     R = unique if pool_rows is None else int(pool_rows)
     assert R >= unique, "pool too small"
-    q = _randn((batch, heads, D) if q_len == 1 else (batch, q_len, heads, D), g, dtype)
+    gv = _value_gen(seed, g, device)
+    q = _randn((batch, heads, D) if q_len == 1 else (batch, q_len, heads, D), gv, dtype)
     perm = torch.randperm(R, generator=g).to(torch.int64)
     pt = torch.empty((batch, seq_len), dtype=torch.int64)
     nxt = 0
@@ -173,16 +189,17 @@ def mla_case(*, batch: int, heads: int, seq_len: int, prefix_len: int = 0,
         n = seq_len - prefix_len
         pt[b, prefix_len:] = perm[nxt:nxt + n]
         nxt += n
-    used = perm[:nxt]
-    pool = torch.zeros((R, 1, 1, D), dtype=_DT[dtype])
-    vals = _randn((nxt, D), g, dtype)
+    used = perm[:nxt].to(q.device)
+    pool = torch.zeros((R, 1, 1, D), dtype=_DT[dtype], device=q.device)
+    vals = _randn((nxt, D), gv, dtype)
     pool.view(R, D).index_copy_(0, used, vals)
     del vals
     # shared-prefix description for decode_plan_prefix: consecutive groups
     meta = {"prefix_group": [b // group if prefix_len > 0 else -1 for b in range(batch)],
             "prefix_len": [prefix_len if prefix_len > 0 else 0] * batch}
-    return DecodeCase(name, q, pool, pool, pt.to(torch.int32),
-                      torch.full((batch,), seq_len, dtype=torch.int32), heads, 1, D, DV,
+    return DecodeCase(name, q, pool, pool, pt.to(torch.int32).to(q.device),
+                      torch.full((batch,), seq_len, dtype=torch.int32, device=q.device),
+                      heads, 1, D, DV,
                       1, D, D, float(scale if scale is not None else 1.0 / math.sqrt(D)),
                       dtype, True, splits, unique_rows=unique, meta=meta, q_len=q_len)
 
@@ -203,25 +220,28 @@ def _qsuffix(q_len: int) -> str:
     return "" if q_len == 1 else f"_q{q_len}"
 
 
-def gqa_tiny(seed: int = 1001, q_len: int = 1) -> DecodeCase:
+def gqa_tiny(seed: int = 1001, q_len: int = 1, device: str = "cpu") -> DecodeCase:
     """Batch 1, 4 query heads on 1 KV head, d 128, 512 tokens, page 16,
     32 pages shuffled in a pool of 32, 4 KV splits."""
     return gqa_case(batch=1, heads=4, kv_heads=1, head_dim=128, page_size=16,
                     seq_lens=[512], pool_pages=32, seed=seed, splits=4,
-                    name="gqa_tiny_b1_h4kv1_d128_L512" + _qsuffix(q_len), q_len=q_len)
+                    name="gqa_tiny_b1_h4kv1_d128_L512" + _qsuffix(q_len), q_len=q_len,
+                    device=device)
 
 
-def gqa_long(context: int, seed: Optional[int] = None, q_len: int = 1) -> DecodeCase:
+def gqa_long(context: int, seed: Optional[int] = None, q_len: int = 1,
+             device: str = "cpu") -> DecodeCase:
     """Batch 1, 16 query heads over 2 KV heads (group 8), d 256, page 16,
     pool = context/16 pages in random order."""
     return gqa_case(batch=1, heads=16, kv_heads=2, head_dim=256, page_size=16,
                     seq_lens=[context], seed=1002 + context if seed is None else seed,
-                    name=f"gqa_long_b1_h16kv2_d256_L{context}" + _qsuffix(q_len), q_len=q_len)
+                    name=f"gqa_long_b1_h16kv2_d256_L{context}" + _qsuffix(q_len), q_len=q_len,
+                    device=device)
 
 
 def mla16(batch: int, seed: Optional[int] = None, context: int = MLA16_CONTEXT,
           prefix: int = MLA16_PREFIX, pool_rows: int = MLA16_POOL_ROWS,
-          splits: Optional[int] = None, q_len: int = 1) -> DecodeCase:
+          splits: Optional[int] = None, q_len: int = 1, device: str = "cpu") -> DecodeCase:
     """16 heads on one 576-wide latent row, page 1, 68,000-token contexts whose
     first 63,240 tokens are shared by groups of 8, a 2,000,000-row pool
     (over 2 GiB, so 64-bit offsets), splits = 256 // batch."""
@@ -230,28 +250,31 @@ def mla16(batch: int, seed: Optional[int] = None, context: int = MLA16_CONTEXT,
                     seed=1003 + batch if seed is None else seed,
                     splits=max(1, 256 // batch) if splits is None else splits,
                     name=f"mla16_b{batch}_L{context}_prefix{prefix}" + _qsuffix(q_len),
-                    q_len=q_len)
+                    q_len=q_len, device=device)
 
 
 def mla_many(heads: int, batch: int, seed: Optional[int] = None,
-             context: int = MLA_MANY_CONTEXT, q_len: int = 1) -> DecodeCase:
+             context: int = MLA_MANY_CONTEXT, q_len: int = 1,
+             device: str = "cpu") -> DecodeCase:
     """nhead 64/128 on the 576-wide latent row, page 1, 16,384 distinct
     tokens per request."""
     return mla_case(batch=batch, heads=heads, seq_len=context, prefix_len=0,
                     seed=1004 + heads + batch if seed is None else seed,
-                    name=f"mla_h{heads}_b{batch}_L{context}" + _qsuffix(q_len), q_len=q_len)
+                    name=f"mla_h{heads}_b{batch}_L{context}" + _qsuffix(q_len), q_len=q_len,
+                    device=device)
 
 
 def gqa_varlen(dtype: str = "bf16", seed: Optional[int] = None,
                lens: Sequence[int] = VARLEN_LENS,
-               pool_pages: Optional[int] = VARLEN_POOL_PAGES, q_len: int = 1) -> DecodeCase:
+               pool_pages: Optional[int] = VARLEN_POOL_PAGES, q_len: int = 1,
+               device: str = "cpu") -> DecodeCase:
     """Batch 10, 32 query heads over 8 KV heads, d 128, page 16, the varlen
     context mix, pages scattered over a 300K-token pool."""
     return gqa_case(batch=len(lens), heads=32, kv_heads=8, head_dim=128,
                     page_size=16, seq_lens=list(lens), pool_pages=pool_pages,
                     dtype=dtype, seed=(1005 if dtype == "bf16" else 1105) if seed is None else seed,
                     name=f"gqa_varlen_{dtype}_b{len(lens)}_h32kv8_d128" + _qsuffix(q_len),
-                    q_len=q_len)
+                    q_len=q_len, device=device)
 
 
 def prefill_case(*, batch: int, heads: int, kv_heads: int, seq_len: int, dtype: str = "bf16",

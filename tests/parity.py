@@ -32,9 +32,26 @@ def oracle_full(case):
 
 
 def oracle_pairs(case, pairs):
+    """The oracle on the listed (b, v) rows, spread over the host's threads
+    (each chunk of rows is one call into the C oracle, which drops the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
     P = oracle.problem(**W.oracle_problem_kwargs(case))
-    return oracle.decode(P, case.q, case.k_pages, case.v_pages, case.page_table,
-                         case.seq_lens, pairs=pairs)
+    pairs = list(pairs)
+    n = max(1, min(THREADS, len(pairs)))
+    chunks = [pairs[i::n] for i in range(n)]
+
+    def run(ch):
+        return oracle.decode(P, case.q, case.k_pages, case.v_pages, case.page_table,
+                             case.seq_lens, pairs=ch)
+
+    with ThreadPoolExecutor(n) as ex:
+        res = list(ex.map(run, chunks))
+    out = np.zeros((len(pairs), case.head_dim_v))
+    lse = np.zeros((len(pairs),))
+    for i, (o, l) in enumerate(res):
+        out[i::n] = o
+        lse[i::n] = l
+    return out, lse
 
 
 def run_gpu(case, dev_case=None, poison=True, **plan_kw):
@@ -91,11 +108,26 @@ def sample_pairs(case, n, seed=0):
     return sorted(pairs)
 
 
-def check_sampled(case, n=8, dev_case=None, **plan_kw):
-    """Full-size run on the GPU, the oracle on n sampled (b, h) heads."""
+def edge_pairs(case, extra=8, seed=0):
+    """Rows of a full-size case the oracle checks one by one: every (query
+    token, head) row of the first and the last request, the first and last
+    row of every request, and `extra` random rows. A fault confined to one
+    head block, one request of a group or a late split shows up in one of
+    them."""
+    B, H = case.batch, case.q_len * case.heads
+    pairs = {(b, h) for b in (0, B - 1) for h in range(H)}
+    pairs |= {(b, h) for b in range(B) for h in (0, H - 1)}
+    pairs |= set(sample_pairs(case, extra, seed))
+    return sorted(pairs)
+
+
+def check_sampled(case, n=8, dev_case=None, pairs=None, **plan_kw):
+    """Full-size run on the GPU, the oracle on n sampled (b, h) heads (or on
+    the given pairs)."""
     out, lse, plan = run_gpu(case, dev_case=dev_case, **plan_kw)
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
-    pairs = sample_pairs(case, n)
+    if pairs is None:
+        pairs = sample_pairs(case, n)
     ref_o, ref_l = oracle_pairs(case, pairs)
     got_o = np.stack([out[b, h] for b, h in pairs])
     got_l = np.array([lse[b, h] for b, h in pairs])

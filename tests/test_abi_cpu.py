@@ -133,7 +133,13 @@ def test_variant_resolution(L):
     assert info["block_tokens"] == 64 and info["stage1_threads"] == 416
     assert _plan(2, 128, 1, 576, 1, seq=[1023, 4096])[0]["variant"] == 3
     assert _plan(1, 48, 1, 576, 1, seq=[4096])[0]["variant"] == 3
-    assert _plan(1, 64, 1, 576, 1, seq=[100], variant="mla_tc")[0]["variant"] == 4
+    assert _plan(1, 64, 1, 576, 1, seq=[1024], variant="mla_tc")[0]["variant"] == 4
+    # its one-part P is refused below 1,024 tokens (empty requests do not count)
+    for seq in ([100], [1023, 4096], [4096, 1]):
+        with pytest.raises(_lib.PkvdError) as e:
+            _plan(len(seq), 64, 1, 576, 1, seq=seq, variant="mla_tc")
+        assert e.value.code == _lib.PKVD_EUNSUPPORTED
+    assert _plan(2, 64, 1, 576, 1, seq=[0, 2048], variant="mla_tc")[0]["variant"] == 4
 
 
 def test_tensor_memory_split_choice(L):
@@ -199,35 +205,79 @@ def _prefix_plan(B, heads, seq, groups, plen, **kw):
     return decode_plan_prefix_compute(make_desc(B, heads, 1, 576, 1, **kw), seq, groups, plen)
 
 
-def test_shared_prefix_plan_covers_every_token_once(L):
-    seq = [1000, 1000, 1000, 500, 800, 900, 64]
-    groups = [0, 0, 0, 1, 1, -1, 2]
-    plen = [700, 700, 700, 300, 300, 0, 64]
-    info, pre, rest = _prefix_plan(7, 16, seq, groups, plen)
-    assert info["num_prefix_items"] == len(pre) > 0 and info["num_items"] == len(rest)
+def _check_prefix_cover(seq, groups, plen, info, pre, rest):
+    """Every token of every request is covered exactly once, by grouped
+    prefix items (members b0 .. b0 + unit - 1) or by its own items; returns
+    the prefix splits of each request."""
+    B = len(seq)
+    assert info["num_prefix_items"] == len(pre) and info["num_items"] == len(rest)
     assert all(g == 1 and 1 <= u <= 4 for (_, u, _, _, _, _, g) in pre)
     assert all(g == 0 for (*_, g) in rest)
-    # members of a grouped item are the consecutive requests b .. b + unit - 1
-    cover = {b: [] for b in range(7)}
-    prefix_splits = {b: set() for b in range(7)}
+    cover = {b: [] for b in range(B)}
+    prefix_splits = {b: set() for b in range(B)}
     for (b0, unit, s, _, t0, t1, _) in pre:
         for b in range(b0, b0 + unit):
             assert groups[b] == groups[b0] and t1 <= plen[b]
             cover[b].append((t0, t1))
             prefix_splits[b].add(s)
-    for (b, _, s, row, t0, t1, _) in rest:
-        assert t0 >= plen[b]
-        cover[b].append((t0, t1))
-    for b in range(7):
+    for (b, u, s, row, t0, t1, _) in rest:
+        if u == 0:   # every head block of a request walks the same tokens
+            cover[b].append((t0, t1))
+    for b in range(B):
         got = sorted(cover[b])
+        if seq[b] == 0:
+            assert not got
+            continue
         assert got[0][0] == 0 and got[-1][1] == seq[b]
         for x, y in zip(got, got[1:]):
             assert x[1] == y[0]
         assert prefix_splits[b] == set(range(len(prefix_splits[b])))
     # partial rows: each request's prefix splits, then its private splits
-    nrows = sum(len(prefix_splits[b]) for b in range(7)) + len(rest)
-    assert info["num_partial_rows"] == nrows
-    assert len({row for (_, _, _, row, _, _, _) in rest}) == len(rest)
+    nrows = sum(len(prefix_splits[b]) for b in range(B)) + len(rest)
+    assert info["num_partial_rows"] == nrows - len(rest) + len([r for r in rest if r[1] == 0])
+    assert len({row for (_, u, _, row, _, _, _) in rest if u == 0}) == \
+        len([r for r in rest if r[1] == 0])
+    return prefix_splits
+
+
+def test_shared_prefix_plan_covers_every_token_once(L):
+    seq = [3000, 3000, 3000, 1500, 2000, 2100, 1100, 900, 900]
+    groups = [0, 0, 0, 1, 1, -1, 2, 3, 3]
+    plen = [1700, 1700, 1700, 1200, 1200, 0, 1100, 500, 500]
+    info, pre, rest = _prefix_plan(len(seq), 16, seq, groups, plen)
+    splits = _check_prefix_cover(seq, groups, plen, info, pre, rest)
+    assert info["num_prefix_items"] > 0
+    # group 3's 500-token prefix is too short to group: read per request
+    assert not splits[7] and not splits[8]
+    assert all(splits[b] for b in range(7) if b != 5)
+    # no prefix split but a prefix's last is shorter than 1,024 tokens
+    for (b0, _, _, _, t0, t1, _) in pre:
+        assert t1 - t0 >= 1024 or t1 == plen[b0]
+
+
+@pytest.mark.parametrize("prefix", [1, 64, 500, 1023])
+def test_short_shared_prefix_is_not_grouped(L, prefix):
+    # the grouped items run on the tensor-memory kernel, whose one-part P is
+    # kept to long items: a short prefix is read by each request itself
+    seq = [prefix + 300, prefix + 300, prefix + 7, prefix]
+    groups, plen = [0] * 4, [prefix] * 4
+    for heads in (16, 64):
+        info, pre, rest = _prefix_plan(4, heads, seq, groups, plen)
+        assert info["num_prefix_items"] == 0 and not pre
+        assert info["variant"] == 3   # mma.sync with its two-part P
+        _check_prefix_cover(seq, groups, plen, info, pre, rest)
+
+
+def test_shared_prefix_private_variant(L):
+    # long prefixes, short private tails: the grouped prefix items go to the
+    # tensor-memory kernel and the tails to the mma.sync kernel
+    info, pre, rest = _prefix_plan(2, 64, [5000, 5000], [0, 0], [4990, 4990])
+    assert info["num_prefix_items"] > 0 and info["variant"] == 3
+    info, pre, rest = _prefix_plan(2, 64, [9000, 9000], [0, 0], [4000, 4000])
+    assert info["num_prefix_items"] > 0 and info["variant"] == 4
+    with pytest.raises(_lib.PkvdError) as e:   # a forced tensor-memory tail that is too short
+        _prefix_plan(2, 64, [5000, 5000], [0, 0], [4990, 4990], variant="mla_tc")
+    assert e.value.code == _lib.PKVD_EUNSUPPORTED
 
 
 def test_shared_prefix_units_of_four_requests(L):

@@ -36,11 +36,15 @@ def test_mla16_batch1_full_size(cuda_ok):
 
 @pytest.mark.parametrize("batch", [8, 48])
 def test_mla16_shared_prefix_full_size(cuda_ok, batch):
+    # every head of the first and last request, the first and last head of
+    # every request (each member of every prefix group), a few random rows
     case = W.mla16(batch)
-    Pt.check_sampled(case, n=6)
+    Pt.check_sampled(case, pairs=Pt.edge_pairs(case))
 
 
-@pytest.mark.parametrize("heads,batch", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("heads,batch", [(64, 64), (64, 128), (128, 64), (128, 128)])
 def test_mla_many_heads_full_size(cuda_ok, heads, batch):
+    # 128 heads: both 64-head items of the first and last request in full
     case = W.mla_many(heads, batch)
-    Pt.check_sampled(case, n=8)
+    res, plan = Pt.check_sampled(case, pairs=Pt.edge_pairs(case))
+    assert plan.info["variant"] == 4

@@ -1,11 +1,11 @@
 """GPU parity of the tensor-memory MLA kernel (tcgen05, 64-head blocks).
 
-It rounds P to one 16-bit value before the P.V product, so at short contexts
-its error against the oracle is bounded by that rounding rather than by the
-output tolerance: each weight p_t carries a relative error of at most 2^-8
-(bf16; 2^-11 for fp16), hence |out - oracle| <= 2^-8 * max_t |v_t - out|.
-The planner only picks it on its own (AUTO) when every request has at least
-1,024 tokens; there the errors average out and the standard tolerances hold.
+It rounds P to one 16-bit value before the P.V product. The planner takes
+it (AUTO) and accepts it (forced) only when every non-empty request has at
+least 1,024 tokens, where the rounding errors average out far below the
+output tolerance; shorter requests are refused for it and run on the
+mma.sync kernel with its two-part P. Every test here holds the standard
+tolerances.
 """
 import math
 
@@ -14,15 +14,10 @@ import pytest
 import torch
 
 import parity as Pt
+from paged_kv_cache_plan_gb300 import _lib
 from paged_kv_cache_plan_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
-
-
-def _one_part_p_bound(case):
-    u = 2.0 ** -8 if case.dtype == "bf16" else 2.0 ** -11
-    vmax = float(case.k_pages.float().abs().max())
-    return 2.0 * vmax * u + Pt.OUT_ATOL
 
 
 @pytest.mark.parametrize("heads,batch,seq_len", [(64, 2, 2048), (128, 2, 1500), (64, 3, 1089)])
@@ -45,14 +40,20 @@ def test_fp16(cuda_ok):
     Pt.check_case(case, variant="mla_tc")
 
 
-@pytest.mark.parametrize("seq_len", [1, 2, 63, 64, 65, 129, 700])
-def test_short_lengths_within_rounding_bound(cuda_ok, seq_len):
+@pytest.mark.parametrize("seq_len", [1, 2, 63, 64, 65, 129, 700, 1023])
+def test_short_lengths_refused_then_auto_within_tolerance(cuda_ok, seq_len):
     case = W.mla_case(batch=2, heads=64, seq_len=seq_len, pool_rows=2 * seq_len + 40, seed=104)
-    out, lse, _ = Pt.run_gpu(case, variant="mla_tc")
-    ref_o, ref_l = Pt.oracle_full(case)
-    assert np.all(np.isfinite(out))
-    assert np.abs(lse - ref_l).max() <= Pt.LSE_ATOL
-    assert np.abs(out - ref_o).max() <= _one_part_p_bound(case)
+    with pytest.raises(_lib.PkvdError) as e:
+        Pt.run_gpu(case, variant="mla_tc")
+    assert e.value.code == _lib.PKVD_EUNSUPPORTED
+    res, plan = Pt.check_case(case)   # AUTO: the mma.sync kernel, standard tolerances
+    assert plan.info["variant"] == 3
+
+
+def test_split_shorter_than_a_block(cuda_ok):
+    # a forced split count that leaves the last split a handful of tokens
+    case = W.mla_case(batch=2, heads=64, seq_len=1100, pool_rows=2300, seed=107)
+    Pt.check_case(case, variant="mla_tc", splits=16)
 
 
 def test_empty_request(cuda_ok):

@@ -5,8 +5,10 @@ the merge combines both kinds of partials. Checked against the oracle (which
 knows nothing of the grouping) and against the plain plan."""
 import numpy as np
 import pytest
+import torch
 
 import parity as Pt
+from paged_kv_cache_plan_gb300 import _lib, plan_for_case, run_case
 from paged_kv_cache_plan_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -42,8 +44,61 @@ def test_fp16(cuda_ok):
     _check_prefix(case)
 
 
+@pytest.mark.parametrize("prefix", [1, 64, 500, 1023])
+@pytest.mark.parametrize("heads", [16, 64])
+def test_short_prefixes_with_private_tails(cuda_ok, prefix, heads):
+    # too short to batch on the tensor-memory kernel: every member reads the
+    # prefix itself, on the mma.sync kernel, at the standard tolerances
+    case = W.mla_case(batch=5, heads=heads, seq_len=prefix + 700, prefix_len=prefix, group=3,
+                      seed=114 + prefix)
+    out, lse, plan = Pt.run_gpu(case, shared_prefix=True)
+    assert plan.info["num_prefix_items"] == 0 and plan.info["variant"] == 3
+    ref_o, ref_l = Pt.oracle_full(case)
+    Pt.compare(out, lse, ref_o, ref_l, case.name + " short shared prefix")
+
+
+def test_long_prefix_short_tails(cuda_ok):
+    # 64 heads: the prefix items on the tensor-memory kernel, 1- to 40-token
+    # private tails on the mma.sync kernel
+    case = W.mla_case(batch=4, heads=64, seq_len=2100, prefix_len=2060, group=4, seed=118)
+    case.seq_lens[:] = torch.tensor([2061, 2070, 2100, 2060], dtype=torch.int32)
+    res = _check_prefix(case)
+
+
+def test_prefix_page_relabelling_bit_exact(cuda_ok):
+    case = W.mla_case(batch=6, heads=16, seq_len=2500, prefix_len=1800, group=3,
+                      pool_rows=9000, seed=119)
+    o1, l1, p1 = Pt.run_gpu(case, shared_prefix=True)
+    assert p1.info["num_prefix_items"] > 0
+    for seed in (1, 2):
+        o2, l2, _ = Pt.run_gpu(W.permute_pages(case, seed), shared_prefix=True)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2), f"relabelling {seed}"
+
+
+def test_prefix_promise_checked(cuda_ok):
+    # with checks on, a member whose prefix page differs from the first
+    # member's is reported (PKVD_EDEVICE_CHECK); the same plan without the
+    # difference reports nothing
+    case = W.mla_case(batch=4, heads=16, seq_len=1500, prefix_len=1200, group=4,
+                      pool_rows=7000, seed=120)
+    dev = case.to("cuda")
+    plan = plan_for_case(case, shared_prefix=True, checks=True)
+    assert plan.info["num_prefix_items"] > 0
+    out = torch.empty((4, 16, 512), device="cuda")
+    lse = torch.empty((4, 16), device="cuda")
+    run_case(plan, dev, out, lse)
+    assert plan.last_device_status() == _lib.PKVD_OK
+    bad = case.page_table.clone()
+    bad[2, 700] = int(case.page_table[2, 1300])   # still inside the pool
+    dev.page_table = bad.cuda()
+    run_case(plan, dev, out, lse)
+    assert plan.last_device_status() == _lib.PKVD_EDEVICE_CHECK
+
+
 @pytest.mark.parametrize("batch", [8, 48])
 def test_mla16_shared_prefix_full_size(cuda_ok, batch):
+    # every head of the first and last request, the first and last head of
+    # every request (each member of every group), a few random rows
     case = W.mla16(batch)
-    res, plan = Pt.check_sampled(case, n=8, shared_prefix=True)
+    res, plan = Pt.check_sampled(case, pairs=Pt.edge_pairs(case), shared_prefix=True)
     assert plan.info["num_prefix_items"] > 0
