@@ -239,6 +239,53 @@ int decode_plan_prefix_compute(const pkvd_plan_desc *desc, const int32_t *seq_le
                                const int32_t *prefix_group, const int32_t *prefix_len,
                                pkvd_plan_info *info, pkvd_work_item *items, int64_t capacity);
 
+/* ------------------------------------------------------------------------
+ * Context-parallel decode: one request's tokens spread over `world` GPUs
+ * (ranks), each holding the whole paged cache and page table. Rank r of
+ * world takes of request b the contiguous token range [begin, begin + len)
+ * with ceil(ceil(L_b / world) / page_size) pages per rank from the start
+ * (ranges start on page boundaries; trailing ranks may be empty). Each rank
+ * runs an ordinary decode over its range (decode_plan_cp + decode_run) and
+ * gets a normalised output and its log-sum-exp per (request, head); the
+ * ranks exchange those rows (an all-gather, the caller's collective) and
+ * decode_merge_ranks combines them into the whole-context result. One query
+ * token per request (q_len 0 or 1); no shared-prefix plans.
+ * Defined by: aiter pull 4758, Technical Details 3 (the split partials'
+ * log-sum-exp merge: here the ranks' ranges are the splits).
+ *
+ * decode_cp_ranges: the token range of every request on rank `rank` (host,
+ * no CUDA call); begin and len are host arrays of `batch` entries. PKVD_EINVAL
+ * for world outside 1 .. 1024, rank outside 0 .. world - 1 or a negative
+ * length. */
+int decode_cp_ranges(int world, int rank, int batch, int page_size, const int32_t *seq_lens,
+                     int32_t *begin, int32_t *len);
+
+/* A plan of rank `rank`'s token ranges (on the current device): seq_lens are
+ * the whole requests' lengths, and decode_run of this plan takes the whole
+ * page table and writes the range's normalised out and lse (an empty range:
+ * out 0, lse -inf). The variant is chosen on the range lengths. Errors as
+ * decode_plan_ex, and PKVD_EINVAL for a bad world or rank, PKVD_EUNSUPPORTED
+ * for q_len > 1. */
+int decode_plan_cp(pkvd_plan **out, const pkvd_plan_desc *desc, const int32_t *seq_lens,
+                   int world, int rank);
+
+/* Host-only planning of decode_plan_cp (no CUDA call; desc->num_sms and
+ * desc->ctas_per_sm must be set), items in grid order with absolute token
+ * positions. Capacity as decode_plan_compute. */
+int decode_plan_cp_compute(const pkvd_plan_desc *desc, const int32_t *seq_lens, int world,
+                           int rank, pkvd_plan_info *info, pkvd_work_item *items,
+                           int64_t capacity);
+
+/* Merge n_ranks ranks' rows: o_parts [n_ranks, rows, dv] fp32 and lse_parts
+ * [n_ranks, rows] fp32 natural log (device, o 16-byte aligned) into out
+ * [rows, dv] and lse [rows]; rows = batch * heads. Ranks are summed in rank
+ * order, so the bits do not depend on which rank merges. dv a multiple of 4
+ * up to 512 (PKVD_EUNSUPPORTED otherwise); PKVD_EINVAL for bad sizes or
+ * pointers, PKVD_ECUDA if the launch failed. Asynchronous on `stream`,
+ * allocates nothing. */
+int decode_merge_ranks(int n_ranks, int64_t rows, int dv, const float *o_parts,
+                       const float *lse_parts, float *out, float *lse, pkvd_stream_t stream);
+
 /* Launch stage 1 and the merge on `stream`. q, k_pages, v_pages, page_table,
  * out and lse are device pointers laid out as above. Asynchronous; returns
  * PKVD_EINVAL for a null or misaligned pointer or a plan made on another

@@ -2,7 +2,8 @@
 
 The names match the C entry points: decode_plan, decode_plan_ex,
 decode_plan_prefix, decode_run, decode_run_timed, decode_run_static,
-decode_run_static_status, decode_plan_destroy, decode_workspace_bytes, decode_plan_query,
+decode_run_static_status, decode_cp_ranges, decode_plan_cp, decode_plan_cp_compute,
+decode_merge_ranks, decode_plan_destroy, decode_workspace_bytes, decode_plan_query,
 decode_last_device_status, decode_plan_compute, decode_plan_prefix_compute,
 decode_status_string, decode_selftest_wait_timeout, prefill_d64_run. Every
 step of the computation runs in libpkvd.so's
@@ -86,6 +87,14 @@ SIGNATURES = {
     "decode_run_static": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, _vp, _vp,
                                          _vp, _vp, _vp]),
     "decode_run_static_status": (ctypes.c_int, [_vp]),
+    "decode_cp_ranges": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        _vp, _vp, _vp]),
+    "decode_plan_cp": (ctypes.c_int, [_pp, ctypes.POINTER(PlanDesc), _vp, ctypes.c_int,
+                                      ctypes.c_int]),
+    "decode_plan_cp_compute": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, ctypes.c_int,
+                                              ctypes.c_int, ctypes.POINTER(PlanInfo), _vp, _i64]),
+    "decode_merge_ranks": (ctypes.c_int, [ctypes.c_int, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                          _vp]),
     "decode_selftest_wait_timeout": (ctypes.c_int, [_vp, _i64, _vp]),
     "prefill_d64_run": (ctypes.c_int, [ctypes.POINTER(PrefillDesc), _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp]),

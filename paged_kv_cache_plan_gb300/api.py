@@ -157,6 +157,95 @@ def decode_plan_prefix_compute(desc: PlanDesc, seq_lens: Sequence[int],
     return info.as_dict(), rows[:info.num_prefix_items], rows[info.num_prefix_items:]
 
 
+def cp_ranges(world: int, rank: int, seq_lens: Sequence[int], page_size: int):
+    """Token range of every request on context-parallel rank `rank` of
+    `world` (decode_cp_ranges): (begin list, length list)."""
+    n = len(seq_lens)
+    begin = (ctypes.c_int32 * max(1, n))()
+    length = (ctypes.c_int32 * max(1, n))()
+    check(_lib.lib().decode_cp_ranges(int(world), int(rank), n, int(page_size),
+                                      ctypes.cast(_seq_array(seq_lens), ctypes.c_void_p),
+                                      ctypes.cast(begin, ctypes.c_void_p),
+                                      ctypes.cast(length, ctypes.c_void_p)), "decode_cp_ranges")
+    return list(begin[:n]), list(length[:n])
+
+
+def decode_plan_cp(desc: PlanDesc, seq_lens: Sequence[int], world: int, rank: int) -> Plan:
+    """Plan of rank `rank`'s token ranges of a context-parallel decode."""
+    h = ctypes.c_void_p()
+    check(_lib.lib().decode_plan_cp(ctypes.byref(h), ctypes.byref(desc),
+                                    ctypes.cast(_seq_array(seq_lens), ctypes.c_void_p),
+                                    int(world), int(rank)), "decode_plan_cp")
+    return Plan(h, desc)
+
+
+def decode_plan_cp_compute(desc: PlanDesc, seq_lens: Sequence[int], world: int, rank: int):
+    """Host-only planning of a rank's plan: (info dict, items as (request,
+    unit, split, partial_row, tok_begin, tok_end))."""
+    L = _lib.lib()
+    info = PlanInfo()
+    seq = _seq_array(seq_lens)
+    check(L.decode_plan_cp_compute(ctypes.byref(desc), ctypes.cast(seq, ctypes.c_void_p),
+                                   int(world), int(rank), ctypes.byref(info), None, 0),
+          "decode_plan_cp_compute")
+    items = []
+    if info.num_items > 0:
+        arr = (WorkItem * info.num_items)()
+        check(L.decode_plan_cp_compute(ctypes.byref(desc), ctypes.cast(seq, ctypes.c_void_p),
+                                       int(world), int(rank), ctypes.byref(info),
+                                       ctypes.cast(arr, ctypes.c_void_p), info.num_items),
+              "decode_plan_cp_compute")
+        items = [(w.request, w.unit, w.split, w.partial_row, w.tok_begin, w.tok_end)
+                 for w in arr]
+    return info.as_dict(), items
+
+
+def decode_merge_ranks(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,
+                       lse: torch.Tensor, stream=None) -> None:
+    """Merge the ranks' rows (decode_merge_ranks): o_parts [R, ..., Dv] and
+    lse_parts [R, ...] fp32 CUDA tensors, out [..., Dv] and lse [...]."""
+    R = o_parts.shape[0]
+    dv = o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    for name, t in (("o_parts", o_parts), ("lse_parts", lse_parts), ("out", out), ("lse", lse)):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    if (lse_parts.shape[0] != R or o_parts.numel() != R * rows * dv or out.numel() != rows * dv
+            or lse.numel() != rows):
+        raise ValueError("o_parts [R, rows, Dv], lse_parts [R, rows], out [rows, Dv], lse [rows]")
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    check(_lib.lib().decode_merge_ranks(int(R), int(rows), int(dv), _ptr(o_parts), _ptr(lse_parts),
+                                        _ptr(out), _ptr(lse), ctypes.c_void_p(s)),
+          "decode_merge_ranks")
+
+
+def gather_ranks(o_r: torch.Tensor, lse_r: torch.Tensor, group=None):
+    """All-gather every rank's rows (torch.distributed, the process group's
+    backend: NCCL on GPUs, gloo on the CPU): returns o_parts [R, *o_r.shape],
+    lse_parts [R, *lse_r.shape] in rank order."""
+    import torch.distributed as dist
+    R = dist.get_world_size(group)
+    # concatenated along the first dimension (the form every backend takes)
+    o_parts = torch.empty((R * o_r.shape[0], *o_r.shape[1:]), dtype=o_r.dtype, device=o_r.device)
+    l_parts = torch.empty((R * lse_r.shape[0], *lse_r.shape[1:]), dtype=lse_r.dtype,
+                          device=lse_r.device)
+    dist.all_gather_into_tensor(o_parts, o_r.contiguous(), group=group)
+    dist.all_gather_into_tensor(l_parts, lse_r.contiguous(), group=group)
+    return o_parts.view(R, *o_r.shape), l_parts.view(R, *lse_r.shape)
+
+
+def cp_decode(plan: Plan, q, k_pages, v_pages, page_table, out, lse, group=None,
+              stream=None) -> None:
+    """Context-parallel decode step on this rank: its range (decode_run of a
+    decode_plan_cp plan), the all-gather of every rank's rows, the merge
+    (decode_merge_ranks) into out / lse, identical on every rank."""
+    o_r = torch.empty_like(out)
+    l_r = torch.empty_like(lse)
+    decode_run(plan, q, k_pages, v_pages, page_table, o_r, l_r, stream)
+    o_parts, l_parts = gather_ranks(o_r, l_r, group)
+    decode_merge_ranks(o_parts, l_parts, out, lse, stream)
+
+
 def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 

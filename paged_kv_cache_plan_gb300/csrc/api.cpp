@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "../../include/pkvd.h"
 #include "kernel_configs.h"
@@ -174,26 +175,37 @@ int decode_plan_compute(const pkvd_plan_desc* desc, const int32_t* seq_lens,
 
 namespace {
 
-// Plan creation shared by decode_plan_ex and decode_plan_prefix (prefix
-// arrays null for a plain plan).
+// Plan creation shared by decode_plan_ex, decode_plan_prefix (prefix arrays
+// non-null) and decode_plan_cp (cp_world > 0: the token range of rank
+// cp_rank).
 int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens,
-              const int32_t* prefix_group, const int32_t* prefix_len) {
+              const int32_t* prefix_group, const int32_t* prefix_len, int cp_world = 0,
+              int cp_rank = 0) {
   if (!out || !desc) return PKVD_EINVAL;
   *out = nullptr;
   const bool prefix = prefix_group != nullptr;
+  const bool cp = cp_world > 0;
   // the per-request items' description (a shared-prefix plan resolves their
-  // variant on the private lengths)
+  // variant on the private lengths, a context-parallel plan on its rank's)
   pkvd_plan_desc d;
   int family = 0;
   int rc = prefix ? pkvd::prefix_private_desc(*desc, seq_lens, prefix_group, prefix_len, &d,
                                               &family)
+           : cp   ? pkvd::cp_shard_desc(*desc, seq_lens, cp_world, cp_rank, &d, &family)
                   : pkvd::normalise_desc(*desc, seq_lens, &d, &family);
   if (rc != PKVD_OK) return rc;
+  // the lengths the items cover (page-tile eligibility depends on them)
+  std::vector<int32_t> item_lens(seq_lens, seq_lens + desc->batch);
+  if (cp) {
+    std::vector<int32_t> begin(desc->batch);
+    pkvd::cp_ranges(cp_world, cp_rank, desc->batch, desc->page_size, seq_lens, begin.data(),
+                    item_lens.data());
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKVD_ECUDA;
   pkvd::KernelEntry s1, s1p, s2;
-  if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, seq_lens), &s1))
+  if (!pkvd::stage1_kernel(d, !prefix && pkvd::plan_uses_tiles(d, item_lens.data()), &s1))
     return PKVD_EUNSUPPORTED;
   if (prefix) {
     if (family != PKVD_FAMILY_MLA || !pkvd::mla_tc_kernel(d.dtype, false, &s1p)) return PKVD_EUNSUPPORTED;
@@ -229,6 +241,7 @@ int make_plan(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_le
   if (!p) return PKVD_ENOMEM;
   try {
     rc = prefix ? pkvd::plan_layout_prefix(d, seq_lens, prefix_group, prefix_len, &p->layout)
+         : cp   ? pkvd::plan_layout_cp(d, seq_lens, cp_world, cp_rank, &p->layout)
                 : pkvd::plan_layout(d, seq_lens, &p->layout);
   } catch (const std::bad_alloc&) {
     rc = PKVD_ENOMEM;
@@ -332,6 +345,51 @@ int decode_plan_prefix_compute(const pkvd_plan_desc* desc, const int32_t* seq_le
                 L.items.size() * sizeof(pkvd_work_item));
   }
   return PKVD_OK;
+}
+
+int decode_plan_cp(pkvd_plan** out, const pkvd_plan_desc* desc, const int32_t* seq_lens,
+                   int world, int rank) {
+  if (world < 1) return PKVD_EINVAL;
+  return make_plan(out, desc, seq_lens, nullptr, nullptr, world, rank);
+}
+
+int decode_plan_cp_compute(const pkvd_plan_desc* desc, const int32_t* seq_lens, int world,
+                           int rank, pkvd_plan_info* info, pkvd_work_item* items,
+                           int64_t capacity) {
+  if (!desc || !info) return PKVD_EINVAL;
+  pkvd::PlanLayout L;
+  int rc;
+  try {
+    rc = pkvd::plan_layout_cp(*desc, seq_lens, world, rank, &L);
+  } catch (const std::bad_alloc&) {
+    return PKVD_ENOMEM;
+  }
+  if (rc != PKVD_OK) return rc;
+  *info = L.info;
+  if (items) {
+    if (capacity < L.info.num_items) return PKVD_EINVAL;
+    std::memcpy(items, L.items.data(), L.items.size() * sizeof(pkvd_work_item));
+  }
+  return PKVD_OK;
+}
+
+int decode_cp_ranges(int world, int rank, int batch, int page_size, const int32_t* seq_lens,
+                     int32_t* begin, int32_t* len) {
+  return pkvd::cp_ranges(world, rank, batch, page_size, seq_lens, begin, len);
+}
+
+int decode_merge_ranks(int n_ranks, int64_t rows, int dv, const float* o_parts,
+                       const float* lse_parts, float* out, float* lse, pkvd_stream_t stream) {
+  if (n_ranks < 1 || n_ranks > pkvd::kMaxCpRanks || rows < 0 || rows > 0x7fffffff)
+    return PKVD_EINVAL;
+  if (dv < 4 || dv > 512 || dv % 4 != 0) return PKVD_EUNSUPPORTED;
+  if (rows > 0 && (!o_parts || !lse_parts || !out || !lse)) return PKVD_EINVAL;
+  if (rows > 0 && (!aligned16(o_parts) || !aligned16(out) ||
+                   (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+                   (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return PKVD_EINVAL;
+  return pkvd::launch_merge_ranks(n_ranks, rows, dv, o_parts, lse_parts, out, lse,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int decode_plan(pkvd_plan** out, int batch, int heads, int kv_heads, int head_dim, int page_size,

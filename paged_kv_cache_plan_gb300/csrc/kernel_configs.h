@@ -118,6 +118,9 @@ constexpr int kMlaTcMinContext = 1024;
 // Query tokens per request a plan takes (multi-token decode).
 constexpr int kMaxQueryLen = 8;
 
+// Ranks a context-parallel decode may spread one request over.
+constexpr int kMaxCpRanks = 1024;
+
 // Stage 2 keeps one float4 sum per warp (8 warps) and float4 column of its
 // Dv slice in shared memory.
 constexpr int kMaxSplits = 8192;

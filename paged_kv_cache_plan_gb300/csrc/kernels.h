@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>   // CUtensorMap (type only; the driver is reached through the runtime)
+#include <cuda_runtime.h>
 
 #include <cstdint>
 
@@ -80,6 +81,12 @@ bool mla_tc_kernel(int dtype, bool causal, KernelEntry* e);
 // (batch x rows x Dv slices blocks, rows = q_len x heads) is at most two
 // blocks per SM.
 bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, KernelEntry* e);
+
+// Merge of n context-parallel ranks' normalised rows (o [n][rows][dv], lse
+// [n][rows] natural log) into out [rows][dv], lse [rows]; dv a multiple of 4
+// up to 512. Returns a pkvd_status.
+int launch_merge_ranks(int n, int64_t rows, int dv, const float* o, const float* lse_in,
+                       float* out, float* lse, cudaStream_t stream);
 
 // Stage-1 kernel for a normalised plan description (variant resolved).
 bool stage1_kernel(const pkvd_plan_desc& d, bool tiles, KernelEntry* e);

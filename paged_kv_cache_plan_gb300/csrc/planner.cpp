@@ -493,4 +493,61 @@ int plan_layout_prefix(const pkvd_plan_desc& in, const int32_t* seq_lens,
   return PKVD_OK;
 }
 
+// ---------------------------------------------------------------- context parallel
+
+int cp_ranges(int world, int rank, int batch, int page_size, const int32_t* seq_lens,
+              int32_t* begin, int32_t* len) {
+  if (world < 1 || world > kMaxCpRanks || rank < 0 || rank >= world || batch < 1 ||
+      page_size < 1 || !seq_lens || !begin || !len)
+    return PKVD_EINVAL;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = seq_lens[b];
+    if (L < 0) return PKVD_EINVAL;
+    // whole pages per rank, so that every range starts on a page boundary
+    const int64_t pages = ceil_div(ceil_div(L, world), page_size);
+    const int64_t c = std::max<int64_t>(1, pages) * page_size;
+    const int64_t b0 = std::min<int64_t>(L, rank * c);
+    const int64_t b1 = std::min<int64_t>(L, (rank + 1) * c);
+    begin[b] = static_cast<int32_t>(b0);
+    len[b] = static_cast<int32_t>(b1 - b0);
+  }
+  return PKVD_OK;
+}
+
+int cp_shard_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, int world, int rank,
+                  pkvd_plan_desc* out, int* family) {
+  if (!seq_lens || in.batch < 1) return PKVD_EINVAL;
+  std::vector<int32_t> begin(in.batch), len(in.batch);
+  int rc = cp_ranges(world, rank, in.batch, in.page_size, seq_lens, begin.data(), len.data());
+  if (rc != PKVD_OK) return rc;
+  // the full lengths fix the page-table width; the rank's lengths resolve
+  // the variant
+  pkvd_plan_desc nd;
+  rc = normalise_desc(in, seq_lens, &nd, family);
+  if (rc != PKVD_OK) return rc;
+  if (nd.q_len != 1) return PKVD_EUNSUPPORTED;   // one query token per request
+  nd.variant = in.variant;
+  return normalise_desc(nd, len.data(), out, family);
+}
+
+int plan_layout_cp(const pkvd_plan_desc& in, const int32_t* seq_lens, int world, int rank,
+                   PlanLayout* out) {
+  pkvd_plan_desc nd;
+  int family = 0;
+  int rc = cp_shard_desc(in, seq_lens, world, rank, &nd, &family);
+  if (rc != PKVD_OK) return rc;
+  const int B = in.batch;
+  std::vector<int32_t> begin(B), len(B);
+  cp_ranges(world, rank, B, in.page_size, seq_lens, begin.data(), len.data());
+  rc = plan_layout(nd, len.data(), out);
+  if (rc != PKVD_OK) return rc;
+  // the items walk absolute token positions of the request's page table
+  for (pkvd_work_item& w : out->items) {
+    w.tok_begin += begin[w.request];
+    w.tok_end += begin[w.request];
+    w.query_pos = seq_lens[w.request] - 1;
+  }
+  return PKVD_OK;
+}
+
 }  // namespace pkvd

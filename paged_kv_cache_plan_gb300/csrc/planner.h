@@ -55,4 +55,21 @@ int prefix_private_desc(const pkvd_plan_desc& in, const int32_t* seq_lens,
 int plan_layout_prefix(const pkvd_plan_desc& desc, const int32_t* seq_lens,
                        const int32_t* prefix_group, const int32_t* prefix_len, PlanLayout* out);
 
+// Context parallel (one request's tokens spread over `world` ranks, each
+// GPU holding the whole page table): rank `rank` takes of request b the
+// tokens [begin[b], begin[b] + len[b]), ceil(ceil(L_b / world) / ps) pages
+// per rank from the start (trailing ranks may be empty).
+int cp_ranges(int world, int rank, int batch, int page_size, const int32_t* seq_lens,
+              int32_t* begin, int32_t* len);
+
+// The normalised description of a rank's plan (the full lengths fix the
+// page-table width, the rank's lengths resolve the variant; one query token).
+int cp_shard_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, int world, int rank,
+                  pkvd_plan_desc* out, int* family);
+
+// A rank's plan: plan_layout on the rank's lengths with every item moved to
+// the absolute token positions of its range.
+int plan_layout_cp(const pkvd_plan_desc& in, const int32_t* seq_lens, int world, int rank,
+                   PlanLayout* out);
+
 }  // namespace pkvd

@@ -257,7 +257,50 @@ __global__ void __launch_bounds__(128) merge_cols(const __grid_constant__ Stage2
     a.lse[bh] = empty ? -INFINITY : (m + log2f(ws)) * 0.69314718055994530942f;
 }
 
+// Merge of context-parallel ranks: each rank's decode over its own token
+// range of every request leaves a normalised output row and its natural-log
+// lse; the rows of n ranks are combined by the same log-sum-exp merge (aiter
+// pull 4758, Technical Details 3), one block per (request, query token, head)
+// row and one thread per float4 column, the ranks summed in rank order:
+//     M = max_r lse_r,  w_r = e^(lse_r - M),
+//     out = sum_r w_r o_r / sum_r w_r,  lse = M + ln sum_r w_r.
+// A rank whose range held no token of the request has lse -inf, weight 0.
+__global__ void __launch_bounds__(128) merge_ranks(const float* __restrict__ o,
+                                                   const float* __restrict__ lse_in, int n,
+                                                   int64_t rows, int dv, float* __restrict__ out,
+                                                   float* __restrict__ lse) {
+  const int64_t row = blockIdx.x;
+  const int c = threadIdx.x;   // float4 column
+  const int cols = dv / 4;
+  float m = -INFINITY;
+  for (int r = 0; r < n; ++r) m = fmaxf(m, __ldg(lse_in + r * rows + row));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ws = 0.f;
+  if (m != -INFINITY) {
+    for (int r = 0; r < n; ++r) {
+      const float l = __ldg(lse_in + r * rows + row);
+      if (l == -INFINITY) continue;
+      const float w = expf(l - m);
+      ws += w;
+      if (c < cols) fma4(acc, w, __ldg(reinterpret_cast<const float4*>(o + (r * rows + row) * dv) + c));
+    }
+  }
+  const float inv = m == -INFINITY ? 0.f : 1.f / ws;
+  if (c < cols)
+    reinterpret_cast<float4*>(out + row * dv)[c] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (c == 0) lse[row] = m == -INFINITY ? -INFINITY : m + logf(ws);
+}
+
 }  // namespace
+
+int launch_merge_ranks(int n, int64_t rows, int dv, const float* o, const float* lse_in,
+                       float* out, float* lse, cudaStream_t stream) {
+  if (rows == 0) return PKVD_OK;
+  merge_ranks<<<dim3(static_cast<unsigned>(rows)), dim3(128), 0, stream>>>(o, lse_in, n, rows, dv,
+                                                                        out, lse);
+  return cudaGetLastError() == cudaSuccess ? PKVD_OK : PKVD_ECUDA;
+}
 
 bool stage2_kernel(const pkvd_plan_info& info, int batch, int heads, int dv, KernelEntry* e) {
   const int tiles = info.stage2_tiles > 0 ? info.stage2_tiles : 1;
