@@ -93,15 +93,15 @@ constexpr int kMlaSmemBytes = kBarrierBytes + kMlaStages * kMlaStageBytes + kMla
 // MLA on the fifth-generation tensor cores (tcgen05): a block of 64 query
 // heads per work item, 64-key blocks in two stages. Warps 0-3 copy K/V rows
 // (16-byte cp.async chunks written straight into the 128-byte-swizzled
-// operand layout), warps 4-11 run the softmax, warp 12 issues the MMAs and
-// owns the tensor memory. Shared memory: [align slack][Q tile][2 stages]
+// operand layout), warps 4-11 run the softmax, warp 12 issues the S^T
+// products and owns the tensor memory, warp 13 issues the O^T products. Shared memory: [align slack][Q tile][2 stages]
 // [P tile][barriers and reduction scratch] = the whole 227 KB of a block.
 constexpr int kMlaTcHeads = 64;
 constexpr int kMlaTcBlockTokens = 64;
 constexpr int kMlaTcStages = 2;
 constexpr int kMlaTcLoadWarps = 4;
 constexpr int kMlaTcSoftmaxWarps = 8;
-constexpr int kMlaTcThreads = (kMlaTcLoadWarps + kMlaTcSoftmaxWarps + 1) * 32;   // 416
+constexpr int kMlaTcThreads = (kMlaTcLoadWarps + kMlaTcSoftmaxWarps + 2) * 32;   // 448
 constexpr int kMlaTcSlabBytes = kMlaTcBlockTokens * 128;     // 64 rows x 64 columns
 constexpr int kMlaTcStageBytes = (kMlaDk / 64) * kMlaTcSlabBytes;               // 73,728
 constexpr int kMlaTcQBytes = (kMlaDk / 64) * kMlaTcHeads * 128;                 // 73,728

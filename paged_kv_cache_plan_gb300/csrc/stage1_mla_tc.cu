@@ -32,12 +32,13 @@
 //               t / 8 + 16 i (i < 4), chunk t % 8 of every slab; a slab's
 //               barrier completes when every copying thread's chunks of it
 //               have landed;
-//   warp 12     allocates the tensor memory; one thread issues the MMAs:
-//               O of a block as soon as its P is ready, the 36 S^T products
-//               of the next block in one pass once it has landed (after a
-//               proxy fence: the copies wrote shared memory through the
-//               generic proxy, the tensor cores read it through the async
-//               proxy);
+//   warp 12     allocates the tensor memory; one thread issues each block's
+//               S^T products slab by slab as the slabs land (after a proxy
+//               fence: the copies wrote shared memory through the generic
+//               proxy, the tensor cores read it through the async proxy);
+//   warp 13     one thread issues each block's O^T products as soon as its P
+//               is ready (a separate issuer, so that neither kind of product
+//               waits behind the other's barrier);
 //   warps 4-11  the softmax. Warp w reads the S^T lanes of quarter w % 4 (16
 //               keys) for 32 of the 64 heads. The running maximum per head is
 //               lazy: it is only raised when a block's scores exceed it by
@@ -104,7 +105,8 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   constexpr int SLAB = kMlaTcSlabBytes;       // one 64-column slab of 64 rows
   constexpr int STAGE = kMlaTcStageBytes;
   constexpr int CH = kMlaDk * 2 / 16;         // 72 16-byte chunks per row
-  constexpr int MMA_WARP = kMlaTcLoadWarps + kMlaTcSoftmaxWarps;
+  constexpr int MMA_WARP = kMlaTcLoadWarps + kMlaTcSoftmaxWarps;   // S^T issue, tensor memory
+  constexpr int O_WARP = MMA_WARP + 1;                              // O^T issue
   constexpr int LDT = kMlaTcLoadWarps * 32;   // copying threads
   constexpr int SMX = kMlaTcSoftmaxWarps * 32;
   constexpr int TCOLS = 512;
@@ -128,7 +130,8 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   const uint32_t sfree = bars + 176;        // [2] S^T buffer read out (8 softmax warps)
   const uint32_t pfull = bars + 192;        // P^T written, O rescaled if needed (8 warps)
   const uint32_t odone = bars + 200;        // O of the latest block done (MMA commit)
-  const uint32_t drain = bars + 208;        // every issued MMA done (at exit)
+  const uint32_t drain = bars + 208;        // every S^T product done (at exit)
+  const uint32_t drain_o = bars + 216;      // every O^T product done (at exit)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
   volatile int* resc_flag = reinterpret_cast<volatile int*>(misc + 264);   // [2]
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     mbar_init(pfull, kMlaTcSoftmaxWarps);
     mbar_init(odone, 1);
     mbar_init(drain, 1);
+    mbar_init(drain_o, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -265,77 +269,71 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
     }
     cp_async_wait_all();
-  } else if (warp == MMA_WARP) {
+  } else if (warp == MMA_WARP || warp == O_WARP) {
     // ------------------------------------------------------------ MMA issue
+    // Two issuing threads, so that neither product waits behind the other's
+    // barrier: warp 12 issues each block's S^T slab by slab as its slabs
+    // land, warp 13 each block's O^T as soon as its P is ready. They write
+    // disjoint tensor-memory columns and read different shared memory, and
+    // each commits (and at the end drains) only what it issued itself.
+    // Descriptors are built once; a byte offset d within the first 256 KB of
+    // shared memory moves a descriptor by d / 16 in its start field, so every
+    // product below is one add and one issue (an issuing thread is bound by
+    // its instruction latency, not by the tensor pipe).
     if (lane == 0 && nblk > 0) {
-      // Descriptors are built once; a byte offset d within the first 256 KB
-      // of shared memory moves a descriptor by d / 16 in its start field, so
-      // every MMA below is one add and one issue (the single issuing thread
-      // is bound by its instruction latency, not by the tensor pipe).
-      const uint64_t dq = tc::sdesc(smem_addr(qs), 16, 1024);
-      const uint64_t dk0 = tc::sdesc(smem_addr(stages), 16, 1024);           // K-major
-      const uint64_t dv0 = tc::sdesc(smem_addr(stages), SLAB, 1024);         // MN-major
-      const uint64_t dp = tc::sdesc(smem_addr(ps), SLAB, 1024);
       constexpr uint64_t kStageStep = STAGE >> 4, kSlabStep = SLAB >> 4;
-      int js = 0, jo = 0;   // next S^T block, next O^T block
-      unsigned long long t0 = 0;
-      int idle = 0;
-      while (jo < nblk) {
-        bool progressed = false;
-        if (jo < js && mbar_test(pfull, jo & 1)) {
+      bool ok = true;
+      if (warp == MMA_WARP) {
+        const uint64_t dq = tc::sdesc(smem_addr(qs), 16, 1024);
+        const uint64_t dk0 = tc::sdesc(smem_addr(stages), 16, 1024);   // K-major
+        for (int js = 0; ok && js < nblk; ++js) {
+          // the S^T buffer must have been read out by block js - 2's softmax
+          if (js >= 2) ok = !*abort_flag && mbar_wait(sfree + 8 * (js & 1), ((js >> 1) - 1) & 1);
+          const uint32_t d = tbase + 4 * R + (js & 1) * R;
+          const uint64_t dk = dk0 + (js & 1) * kStageStep;
+#pragma unroll 1
+          for (int c = 0; ok && c < kSlabs; ++c) {
+            ok = mbar_wait(full + 8 * ((js & 1) * kSlabs + c), (js >> 1) & 1);
+            if (!ok) break;
+            // the slab landed through the generic proxy; the tensor cores
+            // read it through the async proxy
+            fence_proxy_async_smem();
+            tc::fence_after();
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc::mma_f16(d, dk + c * kSlabStep + 2 * k, dq + c * kSlabStep + 2 * k, kIdS,
+                          c > 0 || k > 0);
+          }
+          if (ok) tc::commit(sfull + 8 * (js & 1));
+        }
+        // every product this thread issued must be done before the tensor
+        // memory is freed
+        tc::commit(drain);
+        mbar_wait(drain, 0);
+      } else {
+        const uint64_t dv0 = tc::sdesc(smem_addr(stages), SLAB, 1024);   // MN-major
+        const uint64_t dp = tc::sdesc(smem_addr(ps), SLAB, 1024);
+        for (int jo = 0; ok && jo < nblk; ++jo) {
+          ok = !*abort_flag && mbar_wait(pfull, jo & 1);
+          if (!ok) break;
           tc::fence_after();
           const uint64_t dv = dv0 + (jo & 1) * kStageStep;
 #pragma unroll
           for (int t = 0; t < 4; ++t)
 #pragma unroll
             for (int k = 0; k < BLK / 16; ++k)
-              tc::mma_f16(tbase + t * R, dv + t * 2 * kSlabStep + k * (2048 >> 4), dp + k * (2048 >> 4),
-                          kIdO, jo > 0 || k > 0);
+              tc::mma_f16(tbase + t * R, dv + t * 2 * kSlabStep + k * (2048 >> 4),
+                          dp + k * (2048 >> 4), kIdO, jo > 0 || k > 0);
           tc::commit(empty + 8 * (jo & 1));
           tc::commit(odone);
-          ++jo;
-          progressed = true;
         }
-        // S^T of block js: all 36 products in one pass once the whole block
-        // has landed (a copying thread's arrival on the last slab's barrier
-        // comes after all of its copies), behind one proxy fence (the copies
-        // wrote shared memory through the generic proxy, the tensor cores
-        // read it through the async proxy). Issuing slab by slab with the
-        // barrier tests in between measured ~530 cycles per slab against
-        // ~230 for its four products.
-        if (js < nblk && (js < 2 || mbar_test(sfree + 8 * (js & 1), ((js >> 1) - 1) & 1)) &&
-            mbar_test(full + 8 * ((js & 1) * kSlabs + kSlabs - 1), (js >> 1) & 1)) {
-          fence_proxy_async_smem();
-          tc::fence_after();
-          const uint32_t d = tbase + 4 * R + (js & 1) * R;
-          const uint64_t dk = dk0 + (js & 1) * kStageStep;
-#pragma unroll
-          for (int c = 0; c < kSlabs; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc::mma_f16(d, dk + c * kSlabStep + 2 * k, dq + c * kSlabStep + 2 * k, kIdS,
-                          c > 0 || k > 0);
-          tc::commit(sfull + 8 * (js & 1));
-          ++js;
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if (++idle >= 64) {
-          // nothing to issue for a while: check the clock and the other roles
-          const unsigned long long now = global_timer_ns();
-          if (idle == 64) t0 = now;
-          if (*abort_flag || now - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(a.status, kStatusTimeout);
-            break;
-          }
-          __nanosleep(64);
-        }
+        tc::commit(drain_o);
+        mbar_wait(drain_o, 0);
       }
-      // every issued MMA must be done before the tensor memory is freed
-      tc::commit(drain);
-      mbar_wait(drain, 0);
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(a.status, kStatusTimeout);
+      }
     }
     __syncwarp();
   } else {

@@ -130,7 +130,7 @@ def test_variant_resolution(L):
     # tensor-memory MLA kernel: 64-head blocks, only for long contexts by default
     info = _plan(2, 128, 1, 576, 1, seq=[1024, 4096])[0]
     assert info["variant"] == 4 and info["heads_per_unit"] == 64 and info["units_per_request"] == 2
-    assert info["block_tokens"] == 64 and info["stage1_threads"] == 416
+    assert info["block_tokens"] == 64 and info["stage1_threads"] == 448
     assert _plan(2, 128, 1, 576, 1, seq=[1023, 4096])[0]["variant"] == 3
     assert _plan(1, 48, 1, 576, 1, seq=[4096])[0]["variant"] == 3
     assert _plan(1, 64, 1, 576, 1, seq=[1024], variant="mla_tc")[0]["variant"] == 4
