@@ -141,8 +141,7 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
                                                            : PKVD_VARIANT_MLA_MMA;
     if (d.variant != PKVD_VARIANT_MLA_MMA && d.variant != PKVD_VARIANT_MLA_TC)
       return PKVD_EUNSUPPORTED;
-    if (d.variant == PKVD_VARIANT_MLA_TC && (vheads % kMlaTcHeads != 0 || !long_enough))
-      return PKVD_EUNSUPPORTED;
+    if (d.variant == PKVD_VARIANT_MLA_TC && !long_enough) return PKVD_EUNSUPPORTED;
   } else {
     // The mma consumer is faster than the fp32 FMA consumer on every group
     // size measured on GB300 (the FMA path is issue-bound: about five
@@ -190,7 +189,8 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
   I.ctas_per_sm = d.ctas_per_sm;
   if (family == PKVD_FAMILY_MLA) {
     I.heads_per_unit = d.variant == PKVD_VARIANT_MLA_TC ? kMlaTcHeads : kMlaHeads;
-    I.units_per_request = vheads / I.heads_per_unit;
+    // the tensor-memory kernel zero-pads a request's last 64-row unit
+    I.units_per_request = static_cast<int>(ceil_div(vheads, I.heads_per_unit));
   } else {
     I.heads_per_unit = d.q_len * group;
     I.units_per_request = d.kv_heads;
@@ -233,7 +233,7 @@ int plan_layout(const pkvd_plan_desc& in, const int32_t* seq_lens, PlanLayout* o
       // count that minimises waves x (tokens per item + a pipeline fill of
       // two blocks), so that a last, partly filled wave costs little.
       int64_t best = -1;
-      for (int64_t S = 1; S <= 64; ++S) {
+      for (int64_t S = 1; S <= 4 * target; ++S) {
         const int64_t c = std::max<int64_t>(min_chunk, ceil_div(ceil_div(std::max<int64_t>(maxL, 1), S), blk) * blk);
         const int64_t cost = ceil_div(items_for(c), target) * (c + 2 * blk);
         if (best < 0 || cost < best) {

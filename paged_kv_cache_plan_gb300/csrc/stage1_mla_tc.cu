@@ -1,5 +1,7 @@
 // Stage 1 for MLA on the fifth-generation tensor cores (tcgen05): one block
-// per work item (request b, block of 64 query heads, split s; or, for a
+// per work item (request b, block of 64 (query token, head) rows, the last
+// block of a request zero-padded when its rows are not a multiple of 64,
+// split s; or, for a
 // shared-prefix item, the heads of up to 64 / heads consecutive requests
 // over their common prefix, read through the first member's page table,
 // each head's partial going to its own request's partial row); all heads
@@ -22,8 +24,7 @@
 // (K-major, rows = heads), two K/V stages of nine 64-column slabs (one tile
 // serves as the K-major A operand of S^T and as the MN-major A operand of
 // O^T), and the P^T tile (MN-major, rows = keys). Shared memory holds two
-// stages; the S^T products of a block are issued together once all of it
-// has landed.
+// stages.
 //
 // Roles:
 //   warps 0-3   copy each block slab by slab as 16-byte cp.async chunks
@@ -33,9 +34,10 @@
 //               barrier completes when every copying thread's chunks of it
 //               have landed;
 //   warp 12     allocates the tensor memory; one thread issues each block's
-//               S^T products slab by slab as the slabs land (after a proxy
-//               fence: the copies wrote shared memory through the generic
-//               proxy, the tensor cores read it through the async proxy);
+//               S^T products three slabs at a time as the slabs land (after
+//               a proxy fence: the copies wrote shared memory through the
+//               generic proxy, the tensor cores read it through the async
+//               proxy);
 //   warp 13     one thread issues each block's O^T products as soon as its P
 //               is ready (a separate issuer, so that neither kind of product
 //               waits behind the other's barrier);
@@ -166,15 +168,19 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   const int VH = a.q_len * a.heads;
   // Query row r of the item: row unit * 64 + r of the request, or (grouped
   // shared-prefix item) head r % heads of member r / heads; -1 for the unused
-  // rows of a group with fewer members than fit.
+  // rows (past the request's last row when its rows are not a multiple of
+  // 64, or of a group with fewer members than fit).
   auto q_row = [&](int r) -> int64_t {
-    if (!it.grouped) return static_cast<int64_t>(it.request) * VH + it.unit * R + r;
+    if (!it.grouped)
+      return it.unit * R + r < VH ? static_cast<int64_t>(it.request) * VH + it.unit * R + r : -1;
     const int m = r / a.heads;
     return m < it.unit ? static_cast<int64_t>(it.request + m) * a.heads + (r - m * a.heads) : -1;
   };
   // Partial-output row of query row r (-1: unused).
   auto out_row = [&](int r) -> int64_t {
-    if (!it.grouped) return static_cast<int64_t>(it.partial_row) * VH + it.unit * R + r;
+    if (!it.grouped)
+      return it.unit * R + r < VH ? static_cast<int64_t>(it.partial_row) * VH + it.unit * R + r
+                                  : -1;
     const int m = r / a.heads;
     return m < it.unit
                ? static_cast<int64_t>(a.split_base[it.request + m] + it.split) * a.heads +
@@ -183,7 +189,10 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   };
   // Partial-lse index of query row r (head-major lse array; -1: unused).
   auto lse_idx = [&](int r) -> int64_t {
-    if (!it.grouped) return static_cast<int64_t>(it.unit * R + r) * a.lse_stride + it.partial_row;
+    if (!it.grouped)
+      return it.unit * R + r < VH
+                 ? static_cast<int64_t>(it.unit * R + r) * a.lse_stride + it.partial_row
+                 : -1;
     const int m = r / a.heads;
     return m < it.unit ? static_cast<int64_t>(r - m * a.heads) * a.lse_stride +
                              a.split_base[it.request + m] + it.split

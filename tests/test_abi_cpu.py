@@ -142,6 +142,16 @@ def test_variant_resolution(L):
     assert _plan(2, 64, 1, 576, 1, seq=[0, 2048], variant="mla_tc")[0]["variant"] == 4
 
 
+@pytest.mark.parametrize("heads,q_len,units", [(16, 1, 1), (48, 1, 1), (16, 5, 2), (32, 3, 2),
+                                               (80, 1, 2), (128, 1, 2)])
+def test_tensor_memory_units_are_padded(L, heads, q_len, units):
+    # the last 64-row unit of a request may be partly used
+    info, items = _plan(2, heads, 1, 576, 1, seq=[2048, 1500], variant="mla_tc", q_len=q_len)
+    assert info["variant"] == 4 and info["heads_per_unit"] == 64
+    assert info["units_per_request"] == units
+    _check_cover(info, items, [2048, 1500], units)
+
+
 def test_tensor_memory_split_choice(L):
     # one resident block per SM: the split count minimises waves x (tokens + fill)
     info, items = _plan(64, 64, 1, 576, 1, seq=[16384] * 64, variant="mla_tc")
@@ -165,7 +175,7 @@ def test_tensor_memory_split_choice(L):
     (dict(args=(1, 4, 1, 128, 16), max_pages_per_seq=3), _lib.PKVD_EINVAL),
     (dict(args=(1, 32, 1, 128, 16), variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),   # group 32
     (dict(args=(1, 4, 1, 128, 16), variant="mla_mma"), _lib.PKVD_EUNSUPPORTED),
-    (dict(args=(1, 16, 1, 576, 1), variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),    # heads % 64
+    (dict(args=(1, 16, 1, 576, 1), variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),    # 100 tokens
     (dict(args=(1, 8, 2, 128, 16), variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),
 ])
 def test_argument_errors(L, kw, code):
@@ -348,7 +358,7 @@ def test_merge_block_shape_follows_prefix_splits(L):
     ((1, 8, 2, 128, 16), [100], dict(q_len=9), _lib.PKVD_EUNSUPPORTED),  # over 8 tokens
     ((1, 16, 2, 128, 16), [100], dict(q_len=3), _lib.PKVD_EUNSUPPORTED), # 3 x group 8 > 16
     ((1, 8, 2, 128, 16), [100], dict(q_len=2, variant="gqa_fma"), _lib.PKVD_EUNSUPPORTED),
-    ((1, 16, 1, 576, 1), [2048], dict(q_len=2, variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),
+    ((1, 16, 1, 576, 1), [1000], dict(q_len=2, variant="mla_tc"), _lib.PKVD_EUNSUPPORTED),
 ])
 def test_query_token_errors(L, args, seq, kw, code):
     with pytest.raises(_lib.PkvdError) as e:

@@ -29,6 +29,25 @@ def test_long_contexts(cuda_ok, heads, batch, seq_len):
     Pt.check_case(case, variant="mla_tc", splits=3)
 
 
+@pytest.mark.parametrize("heads,q_len,batch,seq_len", [
+    (16, 1, 1, 3000),    # 16 of 64 rows used
+    (32, 1, 2, 1500),
+    (48, 1, 2, 1100),
+    (16, 3, 2, 1200),    # 48 (token, head) rows
+    (32, 3, 1, 2000),    # 96 rows: one full unit and one half-used unit
+    (80, 1, 1, 1024),    # 80 rows: the second unit holds 16
+])
+def test_padded_units(cuda_ok, heads, q_len, batch, seq_len):
+    # a request whose (query token, head) rows are not a multiple of 64: the
+    # last unit's unused rows carry zero queries and write nothing
+    case = W.mla_case(batch=batch, heads=heads, seq_len=seq_len, q_len=q_len,
+                      pool_rows=batch * seq_len + 200, seed=108)
+    res, plan = Pt.check_case(case, variant="mla_tc")
+    assert plan.info["variant"] == 4
+    assert plan.info["units_per_request"] == -(-q_len * heads // 64)
+    Pt.check_case(case, variant="mla_tc", splits=5)
+
+
 def test_auto_picks_tensor_memory_kernel(cuda_ok):
     case = W.mla_case(batch=1, heads=128, seq_len=1024, pool_rows=1100, seed=102)
     res, plan = Pt.check_case(case)
