@@ -27,6 +27,15 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// A 32-bit read-only load that stays where it is written: __ldg loads are
+// invariant, so the compiler may sink them to their first use, which turns a
+// load issued ahead of time into a stall at the use.
+__device__ __forceinline__ int32_t ld_pinned(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // Two adjacent 16-bit values through the read-only path.
 template <typename T>
 __device__ __forceinline__ uint32_t ldg_pair(const T* p) {

@@ -77,12 +77,19 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
   }
   __syncthreads();
 
-  // Pool row of this lane's row (lanes < RPW) of block j; 0 past the end.
-  auto row_of = [&](int j) -> int64_t {
+  // Page id of this lane's row (lanes < RPW) of block j, 0 past the end: a
+  // load issued PF blocks before the row is formed from it (row_at), so its
+  // latency never stalls the warp.
+  auto page_of = [&](int j) -> int {
+    const int tok = it.tok_begin + j * BLK + warp * RPW + lane;
+    if (lane >= RPW || j >= nblk || tok >= it.tok_end) return 0;
+    return ld_pinned(pt + tok / a.page_size);
+  };
+  // Pool row of this lane's row of block j from its page id; 0 past the end.
+  auto row_at = [&](int j, int page) -> int64_t {
     const int tok = it.tok_begin + j * BLK + warp * RPW + lane;
     if (lane >= RPW || j >= nblk || tok >= it.tok_end) return 0;
     const int pidx = tok / a.page_size;
-    int page = __ldg(pt + pidx);
     if (a.checks && (page < 0 || page >= a.num_pool_pages)) {
       atomicOr(a.status, kStatusBadPage);
       page = 0;
@@ -111,13 +118,13 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
     }
   };
 
-  int64_t rows[PF];
+  int pages[PF];
 #pragma unroll
-  for (int i = 0; i < PF; ++i) rows[i] = row_of(i);
+  for (int i = 0; i < PF; ++i) pages[i] = page_of(i);
 #pragma unroll
   for (int i = 0; i < STAGES; ++i) {
-    if (i < nblk) issue(i, rows[i]);
-    rows[i] = row_of(i + PF);
+    if (i < nblk) issue(i, row_at(i, pages[i]));
+    pages[i] = page_of(i + PF);
   }
   int issued = min(nblk, STAGES);
 
@@ -200,10 +207,10 @@ __global__ void __launch_bounds__(kMlaThreads, 2)
           // Every warp is past block j - 1: refill its stage with block j + STAGES - 1.
           if (j >= 1) {
             if (j + STAGES - 1 < nblk) {
-              issue(j + STAGES - 1, rows[(i + STAGES - 1) % PF]);
+              issue(j + STAGES - 1, row_at(j + STAGES - 1, pages[(i + STAGES - 1) % PF]));
               issued = j + STAGES;
             }
-            rows[(i + STAGES - 1) % PF] = row_of(j + STAGES - 1 + PF);
+            pages[(i + STAGES - 1) % PF] = page_of(j + STAGES - 1 + PF);
           }
 
           // Full scores: the four partials in warp order. Keys at or past

@@ -32,7 +32,10 @@
 //               leaves no contiguous tile to move); thread t copies rows
 //               t / 8 + 16 i (i < 4), chunk t % 8 of every slab; a slab's
 //               barrier completes when every copying thread's chunks of it
-//               have landed;
+//               have landed. A stage is refilled once the O^T of the block
+//               two back is complete (releasing it slab pair by slab pair as
+//               the O^T tiles complete measured slower: the early copies
+//               compete with O^T for shared-memory bandwidth);
 //   warp 12     allocates the tensor memory; one thread issues each block's
 //               S^T products three slabs at a time as the slabs land (after
 //               a proxy fence: the copies wrote shared memory through the
@@ -223,13 +226,20 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
     const uint8_t* pool = static_cast<const uint8_t*>(a.k);
     const int64_t pitch_bytes = a.k_pitch * 2;
-    // byte offset of the pool row of block row r of block j; rows past the
-    // item's end repeat its last row (their keys are masked)
-    auto row_off = [&](int j, int r) -> int64_t {
-      int tok = it.tok_begin + j * BLK + r;
-      if (tok >= it.tok_end) tok = it.tok_end - 1;
+    // Token of block row r of block j; rows past the item's end repeat its
+    // last token (their keys are masked).
+    auto tok_of = [&](int j, int r) -> int {
+      const int tok = it.tok_begin + j * BLK + r;
+      return tok < it.tok_end ? tok : it.tok_end - 1;
+    };
+    // The page id of a row is loaded two blocks ahead, before that block's
+    // copies, and its byte offset formed after the next block's copies
+    // (page_of, then off_of), so that the cold page-table read never holds
+    // up the copies being issued.
+    auto page_of = [&](int j, int r) -> int { return ld_pinned(pt + tok_of(j, r) / a.page_size); };
+    auto off_of = [&](int j, int r, int page) -> int64_t {
+      const int tok = tok_of(j, r);
       const int pidx = tok / a.page_size;
-      int page = __ldg(pt + pidx);
       if (a.checks) {
         // a grouped item reads the shared tokens through its first member's
         // page table: the other members must name the same pages
@@ -244,11 +254,18 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
              pitch_bytes;
     };
     // this thread's rows of a block: tid / 8 + 16 i
-    int64_t cur[4], nxt[4];
+    int64_t cur[4];
+    int pg[4];   // page ids of the next block's rows
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cur[i] = nblk > 0 ? row_off(0, tid / 8 + 16 * i) : 0;
+    for (int i = 0; i < 4; ++i) {
+      cur[i] = nblk > 0 ? off_of(0, tid / 8 + 16 * i, page_of(0, tid / 8 + 16 * i)) : 0;
+      pg[i] = nblk > 1 ? page_of(1, tid / 8 + 16 * i) : 0;
+    }
     for (int j = 0; j < nblk; ++j) {
       const int s = j & 1;
+      int pg2[4];   // page ids of block j + 2
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pg2[i] = j + 2 < nblk ? page_of(j + 2, tid / 8 + 16 * i) : 0;
       if (j >= 2) {
         const bool ok = !*abort_flag && mbar_wait(empty + 8 * s, ((j >> 1) - 1) & 1);
         if (!__all_sync(kFull, ok)) {
@@ -258,10 +275,6 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           }
           break;
         }
-      }
-      if (j + 1 < nblk) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) nxt[i] = row_off(j + 1, tid / 8 + 16 * i);
       }
       const uint32_t st = smem_addr(stages + s * STAGE);
       // Each slab is announced asynchronously once this thread's copies of it
@@ -275,15 +288,19 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
                      pool + cur[i] + (8 * c + cq) * 16);
         cp_async_arrive(full + 8 * (s * kSlabs + c));
       }
+      // the next block's offsets from ids loaded a block ago
 #pragma unroll
-      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 4; ++i) {
+        if (j + 1 < nblk) cur[i] = off_of(j + 1, tid / 8 + 16 * i, pg[i]);
+        pg[i] = pg2[i];
+      }
     }
     cp_async_wait_all();
   } else if (warp == MMA_WARP || warp == O_WARP) {
     // ------------------------------------------------------------ MMA issue
     // Two issuing threads, so that neither product waits behind the other's
-    // barrier: warp 12 issues each block's S^T slab by slab as its slabs
-    // land, warp 13 each block's O^T as soon as its P is ready. They write
+    // barrier: warp 12 issues each block's S^T three slabs at a time as its
+    // slabs land, warp 13 each block's O^T as soon as its P is ready. They write
     // disjoint tensor-memory columns and read different shared memory, and
     // each commits (and at the end drains) only what it issued itself.
     // Descriptors are built once; a byte offset d within the first 256 KB of
