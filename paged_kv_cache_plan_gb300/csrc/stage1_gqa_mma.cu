@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
   // The item's query rows [GMAX][D] in padded rows (zero past NQ): the
   // source of the Q^T B fragments, read with ldmatrix each block. Loaded by
   // the whole block once every warp has its first KV copies in flight (all
-  // warps run this exactly once, so the barrier inside is safe).
+  // warps run this exactly once, so the barrier inside is safe), with
+  // cp.async so that all of its loads are in flight together.
   auto load_q = [&]() {
     constexpr int CHUNKS = D * 2 / 16;
     for (int i = threadIdx.x; i < GMAX * CHUNKS; i += gqa_threads(D)) {
@@ -55,11 +56,13 @@ __global__ void __launch_bounds__(gqa_threads(D), NT == 1 ? 2 : 1)
       const int64_t qrow =
           CAUSAL ? (static_cast<int64_t>(it.request) * a.q_len + h / G) * a.heads + kvh * G + h % G
                  : static_cast<int64_t>(it.request) * a.heads + kvh * G + h;
-      *reinterpret_cast<uint4*>(sm.qtile + h * gqa_row_pitch(D) + c * 16) =
-          h < NQ ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) +
-                                                        qrow * D * 2) + c)
-                 : make_uint4(0u, 0u, 0u, 0u);
+      uint8_t* dst = sm.qtile + h * gqa_row_pitch(D) + c * 16;
+      if (h < NQ)
+        cp_async16(smem_addr(dst), static_cast<const uint8_t*>(a.q) + qrow * D * 2 + c * 16);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
+    cp_async_wait_all();
     __syncthreads();
   };
   // Last visible token (relative to the item) of this lane's C-fragment

@@ -201,16 +201,39 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
                              a.split_base[it.request + m] + it.split
                        : -1;
   };
-  // Q tile: the 64 query rows, K-major (unused rows zero).
+  // K/V rows of the item: the request's page table; token of block row r of
+  // block j (rows past the item's end repeat its last token, their keys are
+  // masked). The page ids of a row are read ahead of use (page_of) and turned
+  // into byte offsets later (off_of, in the copying warps).
+  const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
+  auto tok_of = [&](int j, int r) -> int {
+    const int tok = it.tok_begin + j * BLK + r;
+    return tok < it.tok_end ? tok : it.tok_end - 1;
+  };
+  auto page_of = [&](int j, int r) -> int { return ld_pinned(pt + tok_of(j, r) / a.page_size); };
+  // the copying threads' page ids of the first two blocks, read before the
+  // query tile so that the two round trips overlap
+  int pg0[4] = {0, 0, 0, 0}, pg1[4] = {0, 0, 0, 0};
+  if (warp < kMlaTcLoadWarps) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (nblk > 0) pg0[i] = page_of(0, threadIdx.x / 8 + 16 * i);
+      if (nblk > 1) pg1[i] = page_of(1, threadIdx.x / 8 + 16 * i);
+    }
+  }
+  // Q tile: the 64 query rows, K-major (unused rows zero), moved with
+  // cp.async so that all of its loads are in flight together.
   {
     for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
       const int r = i / CH, ch = i - r * CH;
       const int64_t qr = q_row(r);
-      *reinterpret_cast<uint4*>(qs + swz_off(r, ch, SLAB)) =
-          qr >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.q) +
-                                                         qr * (kMlaDk * 2)) + ch)
-                  : make_uint4(0u, 0u, 0u, 0u);
+      if (qr >= 0)
+        cp_async16(smem_addr(qs + swz_off(r, ch, SLAB)),
+                   static_cast<const uint8_t*>(a.q) + qr * (kMlaDk * 2) + ch * 16);
+      else
+        *reinterpret_cast<uint4*>(qs + swz_off(r, ch, SLAB)) = make_uint4(0u, 0u, 0u, 0u);
     }
+    cp_async_wait_all();
     fence_proxy_async_smem();
   }
   if (warp == MMA_WARP) tc::alloc(smem_addr(tslot), TCOLS);
@@ -223,20 +246,12 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     // ------------------------------------------------------------ copies
     const int tid = threadIdx.x;
     const int cq = tid & 7;                          // 16-byte chunk within a slab row
-    const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
     const uint8_t* pool = static_cast<const uint8_t*>(a.k);
     const int64_t pitch_bytes = a.k_pitch * 2;
-    // Token of block row r of block j; rows past the item's end repeat its
-    // last token (their keys are masked).
-    auto tok_of = [&](int j, int r) -> int {
-      const int tok = it.tok_begin + j * BLK + r;
-      return tok < it.tok_end ? tok : it.tok_end - 1;
-    };
     // The page id of a row is loaded two blocks ahead, before that block's
     // copies, and its byte offset formed after the next block's copies
     // (page_of, then off_of), so that the cold page-table read never holds
     // up the copies being issued.
-    auto page_of = [&](int j, int r) -> int { return ld_pinned(pt + tok_of(j, r) / a.page_size); };
     auto off_of = [&](int j, int r, int page) -> int64_t {
       const int tok = tok_of(j, r);
       const int pidx = tok / a.page_size;
@@ -258,8 +273,8 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     int pg[4];   // page ids of the next block's rows
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      cur[i] = nblk > 0 ? off_of(0, tid / 8 + 16 * i, page_of(0, tid / 8 + 16 * i)) : 0;
-      pg[i] = nblk > 1 ? page_of(1, tid / 8 + 16 * i) : 0;
+      cur[i] = nblk > 0 ? off_of(0, tid / 8 + 16 * i, pg0[i]) : 0;
+      pg[i] = pg1[i];
     }
     for (int j = 0; j < nblk; ++j) {
       const int s = j & 1;
@@ -410,6 +425,7 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     for (int j = 0; j < nblk; ++j) {
       const int b = j & 1;
       const bool ok = __all_sync(kFull, !*abort_flag && mbar_wait(sfull + 8 * b, (j >> 1) & 1));
+      const bool o_prev = j == 0 || mbar_test(odone, (j - 1) & 1);
       float x[32];
       bool need = j == 0;
       if (ok) {
@@ -488,13 +504,10 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
         }
         scores(j, b, x);   // read again: the fold consumed the first copy
       }
-      // S^T buffer b is in registers now
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sfree + 8 * b);
       // O of the previous block must be done before P^T is rewritten (a wait
       // that runs out stops the loop at the next vote)
-      if (j >= 1 && !o_ready && !__all_sync(kFull, !*abort_flag && mbar_wait(odone, (j - 1) & 1)))
+      if (j >= 1 && !o_ready &&
+          !__all_sync(kFull, o_prev || (!*abort_flag && mbar_wait(odone, (j - 1) & 1))))
         *abort_flag = 1;
       // P = exp2(s - m); P^T in the inputs' 16-bit type into shared memory
 #pragma unroll
@@ -516,6 +529,10 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(pfull);
+      // S^T buffer b was read out before P
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree + 8 * b);
       // running sums of P in fp32 (the log-sum-exp needs them unrounded)
       {
         tc::fence_after();
