@@ -582,6 +582,11 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
         }
         named_sync(1, SMX);
         tc::fence_after();
+        // the partial rows are staged as [64 rows][512] fp32 in the K/V stages
+        // (idle now: every product is done) and written by bulk copies, one
+        // 2 KB row each, instead of 128 scalar stores per thread
+        float* ostage = reinterpret_cast<float*>(stages);
+        static_assert(R * kMlaDv * 4 <= kMlaTcStages * STAGE, "partial rows fit the stages");
 #pragma unroll 1
         for (int t = 0; t < 4; ++t) {
           uint32_t o[32];
@@ -591,11 +596,20 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = 0u;
           }
-          float* ocol = a.o_part + 128 * t + 32 * q + lane;
+          const int dvi = 128 * t + 32 * q + lane;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int64_t orow = out_row(32 * h + c);
-            if (orow >= 0) ocol[orow * a.dv] = __uint_as_float(o[c]) * alpha_s[32 * h + c];
+          for (int c = 0; c < 32; ++c)
+            ostage[(32 * h + c) * kMlaDv + dvi] = __uint_as_float(o[c]) * alpha_s[32 * h + c];
+        }
+        fence_proxy_async_smem();
+        named_sync(1, SMX);
+        {
+          const int r = threadIdx.x - kMlaTcLoadWarps * 32;
+          if (r < R) {
+            const int64_t orow = out_row(r);
+            if (orow >= 0)
+              bulk_store_s2g(a.o_part + orow * a.dv, smem_addr(ostage + r * kMlaDv), kMlaDv * 4);
+            bulk_store_commit_wait_read();
           }
         }
       }
