@@ -131,14 +131,16 @@ int normalise_desc(const pkvd_plan_desc& in, const int32_t* seq_lens, pkvd_plan_
     // taken (and only accepted) when every non-empty request has at least
     // kMlaTcMinContext tokens, where that rounding averages out far below
     // the output tolerance. Shorter contexts run on the mma.sync kernel,
-    // which keeps a second, low part of P.
+    // which keeps a second, low part of P. Row counts that are not a
+    // multiple of 64 take it too (its last unit zero-padded): with one
+    // product per 64 keys the padding costs little, and it measured faster
+    // than the 16-row mma.sync kernel at 16 heads.
     int64_t min_len = INT64_MAX;
     for (int b = 0; b < d.batch; ++b)
       if (seq_lens[b] > 0) min_len = std::min<int64_t>(min_len, seq_lens[b]);
     const bool long_enough = min_len >= kMlaTcMinContext;
     if (d.variant == PKVD_VARIANT_AUTO)
-      d.variant = vheads % kMlaTcHeads == 0 && long_enough ? PKVD_VARIANT_MLA_TC
-                                                           : PKVD_VARIANT_MLA_MMA;
+      d.variant = long_enough ? PKVD_VARIANT_MLA_TC : PKVD_VARIANT_MLA_MMA;
     if (d.variant != PKVD_VARIANT_MLA_MMA && d.variant != PKVD_VARIANT_MLA_TC)
       return PKVD_EUNSUPPORTED;
     if (d.variant == PKVD_VARIANT_MLA_TC && !long_enough) return PKVD_EUNSUPPORTED;

@@ -244,11 +244,13 @@ def mla16(batch: int, seed: Optional[int] = None, context: int = MLA16_CONTEXT,
           splits: Optional[int] = None, q_len: int = 1, device: str = "cpu") -> DecodeCase:
     """16 heads on one 576-wide latent row, page 1, 68,000-token contexts whose
     first 63,240 tokens are shared by groups of 8, a 2,000,000-row pool
-    (over 2 GiB, so 64-bit offsets), splits = 256 // batch."""
+    (over 2 GiB, so 64-bit offsets). The split count is the planner's own
+    choice unless `splits` forces one (the aiter page's kernel used
+    256 // batch, `splits=max(1, 256 // batch)` reproduces that)."""
     return mla_case(batch=batch, heads=16, seq_len=context, prefix_len=prefix,
                     group=8, pool_rows=pool_rows,
                     seed=1003 + batch if seed is None else seed,
-                    splits=max(1, 256 // batch) if splits is None else splits,
+                    splits=0 if splits is None else splits,
                     name=f"mla16_b{batch}_L{context}_prefix{prefix}" + _qsuffix(q_len),
                     q_len=q_len, device=device)
 

@@ -132,7 +132,10 @@ def test_variant_resolution(L):
     assert info["variant"] == 4 and info["heads_per_unit"] == 64 and info["units_per_request"] == 2
     assert info["block_tokens"] == 64 and info["stage1_threads"] == 448
     assert _plan(2, 128, 1, 576, 1, seq=[1023, 4096])[0]["variant"] == 3
-    assert _plan(1, 48, 1, 576, 1, seq=[4096])[0]["variant"] == 3
+    # row counts that are not a multiple of 64 take it too (padded last unit)
+    info = _plan(1, 48, 1, 576, 1, seq=[4096])[0]
+    assert info["variant"] == 4 and info["units_per_request"] == 1
+    assert _plan(1, 16, 1, 576, 1, seq=[1023])[0]["variant"] == 3
     assert _plan(1, 64, 1, 576, 1, seq=[1024], variant="mla_tc")[0]["variant"] == 4
     # its one-part P is refused below 1,024 tokens (empty requests do not count)
     for seq in ([100], [1023, 4096], [4096, 1]):
@@ -375,7 +378,11 @@ def test_query_tokens_layout(L):
     info, _ = _plan(3, 16, 1, 576, 1, seq=[4096] * 3, q_len=4)
     assert info["variant"] == 4 and info["heads_per_unit"] == 64
     assert info["units_per_request"] == 1
+    # 16 heads x 2 tokens: 32 rows, one zero-padded 64-row unit
     info, _ = _plan(3, 16, 1, 576, 1, seq=[4096] * 3, q_len=2)
+    assert info["variant"] == 4 and info["units_per_request"] == 1
+    # short contexts: the mma.sync kernel's 16-row units
+    info, _ = _plan(3, 16, 1, 576, 1, seq=[900] * 3, q_len=2)
     assert info["variant"] == 3 and info["units_per_request"] == 2
     # the merge runs over batch x q_len x heads rows: 1 x 4 x 16 = 64 rows tile 2 ways
     info, _ = _plan(1, 16, 1, 576, 1, seq=[68000], q_len=4)
