@@ -119,6 +119,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte cp.async that copies `src_bytes` (0 or 16) from global memory and
+// fills the rest of the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {

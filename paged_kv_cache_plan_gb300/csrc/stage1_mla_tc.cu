@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   const uint32_t odone = bars + 200;        // O of the latest block done (MMA commit)
   const uint32_t drain = bars + 208;        // every S^T product done (at exit)
   const uint32_t drain_o = bars + 216;      // every O^T product done (at exit)
+  const uint32_t qfull = bars + 224;        // the Q tile landed (every thread)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(misc + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
   volatile int* resc_flag = reinterpret_cast<volatile int*>(misc + 264);   // [2]
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     mbar_init(odone, 1);
     mbar_init(drain, 1);
     mbar_init(drain_o, 1);
+    mbar_init(qfull, kMlaTcThreads);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -221,26 +223,24 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       if (nblk > 1) pg1[i] = page_of(1, threadIdx.x / 8 + 16 * i);
     }
   }
-  // Q tile: the 64 query rows, K-major (unused rows zero), moved with
-  // cp.async so that all of its loads are in flight together.
-  {
-    for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
-      const int r = i / CH, ch = i - r * CH;
-      const int64_t qr = q_row(r);
-      if (qr >= 0)
-        cp_async16(smem_addr(qs + swz_off(r, ch, SLAB)),
-                   static_cast<const uint8_t*>(a.q) + qr * (kMlaDk * 2) + ch * 16);
-      else
-        *reinterpret_cast<uint4*>(qs + swz_off(r, ch, SLAB)) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
+  // Q tile: the 64 query rows, K-major, moved with cp.async so that all of
+  // its loads are in flight together (an unused row's chunks copy no source
+  // bytes and fill zeros). Nobody waits for it here: every thread arrives on
+  // qfull once its chunks have landed, and only the S^T issue waits, so the
+  // first K/V copies go out while the tile is still on its way.
+  for (int i = threadIdx.x; i < R * CH; i += kMlaTcThreads) {
+    const int r = i / CH, ch = i - r * CH;
+    const int64_t qr = q_row(r);
+    cp_async16_zfill(smem_addr(qs + swz_off(r, ch, SLAB)),
+                     static_cast<const uint8_t*>(a.q) + (qr >= 0 ? qr * (kMlaDk * 2) + ch * 16 : 0),
+                     qr >= 0 ? 16u : 0u);
   }
   if (warp == MMA_WARP) tc::alloc(smem_addr(tslot), TCOLS);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
+  cp_async_arrive(qfull);   // the barrier's initialisation is visible after the sync
 
   if (warp < kMlaTcLoadWarps) {
     // ------------------------------------------------------------ copies
@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       if (warp == MMA_WARP) {
         const uint64_t dq = tc::sdesc(smem_addr(qs), 16, 1024);
         const uint64_t dk0 = tc::sdesc(smem_addr(stages), 16, 1024);   // K-major
+        // the Q tile (fenced for the async proxy below, with the slabs)
+        ok = mbar_wait(qfull, 0);
         for (int js = 0; ok && js < nblk; ++js) {
           // the S^T buffer must have been read out by block js - 2's softmax
           if (js >= 2) ok = !*abort_flag && mbar_wait(sfree + 8 * (js & 1), ((js >> 1) - 1) & 1);
