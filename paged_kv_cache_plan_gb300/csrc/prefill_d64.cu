@@ -267,8 +267,9 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
         break;
       }
       tc::fence_after();
-      // the row's 128 scaled scores, read once (keys after the row's own
-      // position masked on the diagonal tile)
+      // the row's unscaled scores, read once (keys after the row's own
+      // position masked on the diagonal tile); the scale is folded into the
+      // exponent's fused multiply-add below
       const uint32_t ts = tbase + lanes + s * BN;
       float sc[BN];
 #pragma unroll
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
         uint32_t x[32];
         tc::ld32(ts + 32 * c4, x);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sc[32 * c4 + i] = __uint_as_float(x[i]) * sl2;
+        for (int i = 0; i < 32; ++i) sc[32 * c4 + i] = __uint_as_float(x[i]);
       }
       // S buffer s is in registers: the MMA may overwrite it
       tc::fence_before();
@@ -288,14 +289,15 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
           if (j * BN + c > qi) sc[c] = -INFINITY;
       }
       // block maximum as eight independent chains (a single chain of 128
-      // dependent maxima would cost its full latency every tile)
+      // dependent maxima would cost its full latency every tile), on the
+      // unscaled scores (the scale is positive), then scaled
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = sc[k];
 #pragma unroll
       for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sc[c]);
       const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
       bool need = false;
       float alpha = 1.f;
       if (j == 0) {
@@ -306,13 +308,23 @@ __global__ void __launch_bounds__(kThreads, C::MINB)
         m = mb;
         l *= alpha;
       }
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight chains again
+      // P = exp2(s * scale - m): one paired fused multiply-add forms two
+      // exponents, one paired add takes two P into the row sum (four chains
+      // of pairs)
+      {
+        const uint64_t scale2 = f32x2(sl2, sl2), negm2 = f32x2(-m, -m);
+        uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};   // +0.0f pairs
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        sc[c] = ex2(sc[c] - m);
-        ls[c & 7] += sc[c];
+        for (int c = 0; c < BN; c += 2) {
+          const float2 e = f32x2_split(ffma_x2(f32x2(sc[c], sc[c + 1]), scale2, negm2));
+          sc[c] = ex2(e.x);
+          sc[c + 1] = ex2(e.y);
+          ls[(c >> 1) & 3] = fadd_x2(ls[(c >> 1) & 3], f32x2(sc[c], sc[c + 1]));
+        }
+        const float2 l01 = f32x2_split(fadd_x2(ls[0], ls[1]));
+        const float2 l23 = f32x2_split(fadd_x2(ls[2], ls[3]));
+        l += (l01.x + l01.y) + (l23.x + l23.y);
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       // O of tile j - 1 must be complete before its P tile is rewritten and
       // before O is rescaled
       if (j >= 1 && !wait_all(pfree, (j - 1) & 1)) {
