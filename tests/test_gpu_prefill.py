@@ -41,6 +41,15 @@ def test_one_part_rows(cuda_ok):
     Pt.compare(out, lse, *Pt.oracle_full(case), case.name)
 
 
+@pytest.mark.parametrize("seq_len", [1100, 1408, 2300])
+def test_late_tile_counts(cuda_ok, seq_len):
+    # late query tiles (one-part P) in odd and even counts: 1,100 tokens
+    # leave one late tile, 1,408 three, 2,300 ten with a partial last tile
+    case = W.prefill_case(batch=1, heads=2, kv_heads=2, seq_len=seq_len, seed=seq_len)
+    out, lse = _run(case)
+    Pt.compare(out, lse, *Pt.oracle_full(case), case.name)
+
+
 def test_fp16(cuda_ok):
     case = W.prefill_case(batch=1, heads=4, kv_heads=4, seq_len=513, dtype="fp16", seed=5)
     out, lse = _run(case)
