@@ -95,8 +95,10 @@ typedef enum pkvd_variant {
   PKVD_VARIANT_GQA_MMA = 2,   /* mma.sync m16n8k16: keys as M, the head group as N */
   PKVD_VARIANT_MLA_MMA = 3,   /* mma.sync, a block of 16 heads per work item       */
   PKVD_VARIANT_MLA_TC = 4     /* tcgen05 with tensor-memory accumulators, a block
-                                 of 64 heads per work item (heads % 64 == 0); P
-                                 is rounded to one 16-bit value, so it is taken
+                                 of 64 (query token, head) rows per work item,
+                                 the last block of a request zero-padded when
+                                 q_len * heads is not a multiple of 64; P is
+                                 rounded to one 16-bit value, so it is taken
                                  (AUTO) and accepted (forced) only when every
                                  non-empty request has >= 1024 tokens; else
                                  PKVD_EUNSUPPORTED                              */
@@ -133,8 +135,7 @@ typedef struct pkvd_plan_desc {
                                  non-empty request needs L_b >= q_len. GQA: the
                                  mma variant with q_len * heads / kv_heads <= 16
                                  (the FMA variant takes q_len 1 only); MLA: both
-                                 variants (tensor-memory: q_len * heads a
-                                 multiple of 64); no shared-prefix plans          */
+                                 variants; no shared-prefix plans                 */
   int64_t max_pages_per_seq;  /* page_table row stride; 0 = max ceil(L_b / ps)    */
   int64_t num_pool_pages;     /* pages in the pools; 0 = unknown (no checks)      */
   int64_t k_row_pitch;        /* elements between K rows; 0 = D (MLA: 576)        */
