@@ -121,7 +121,6 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
   static_assert(SLAB == R * 128, "the Q tile and the K/V stages share one slab size");
   static_assert(4 * R + 2 * R + 64 <= TCOLS, "tensor memory columns");
   static_assert(LDT == 2 * BLK && kMlaTcSoftmaxWarps == 8, "warp roles");
-  static_assert(kSlabs % 3 == 0, "S^T products are issued three slabs at a time");
 
   extern __shared__ uint8_t raw[];
   uint8_t* sm = raw + ((kTileAlign - (smem_addr(raw) & (kTileAlign - 1))) & (kTileAlign - 1));
@@ -335,21 +334,24 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           if (js >= 2) ok = !*abort_flag && mbar_wait(sfree + 8 * (js & 1), ((js >> 1) - 1) & 1);
           const uint32_t d = tbase + 4 * R + (js & 1) * R;
           const uint64_t dk = dk0 + (js & 1) * kStageStep;
-          // three slabs at a time: a copying thread's arrival on a slab's
-          // barrier comes after all of its earlier copies, so the third
-          // slab's barrier covers the group (one wait and one pair of
-          // fences per group: the issuing thread's own instructions, not the
-          // tensor pipe, set the rate of these small products)
-#pragma unroll 1
-          for (int g = 0; ok && g < kSlabs / 3; ++g) {
-            ok = mbar_wait(full + 8 * ((js & 1) * kSlabs + 3 * g + 2), (js >> 1) & 1);
+          // a few slabs at a time: a copying thread's arrival on a slab's
+          // barrier comes after all of its earlier copies, so the last
+          // slab's barrier of a group covers the group (one wait and one pair
+          // of fences per group: the issuing thread's own instructions, not
+          // the tensor pipe, set the rate of these small products)
+          constexpr int kGroupEnd[] = {2, 5, 8};   // last slab of each group
+          constexpr int kGroups = sizeof(kGroupEnd) / sizeof(kGroupEnd[0]);
+          static_assert(kGroupEnd[kGroups - 1] == kSlabs - 1, "the groups cover the slabs");
+#pragma unroll
+          for (int gr = 0; gr < kGroups; ++gr) {
+            if (ok) ok = mbar_wait(full + 8 * ((js & 1) * kSlabs + kGroupEnd[gr]), (js >> 1) & 1);
             if (!ok) break;
             // the slabs landed through the generic proxy; the tensor cores
             // read them through the async proxy
             fence_proxy_async_smem();
             tc::fence_after();
 #pragma unroll
-            for (int c = 3 * g; c < 3 * g + 3; ++c)
+            for (int c = gr == 0 ? 0 : kGroupEnd[gr - 1] + 1; c <= kGroupEnd[gr]; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 tc::mma_f16(d, dk + c * kSlabStep + 2 * k, dq + c * kSlabStep + 2 * k, kIdS,
