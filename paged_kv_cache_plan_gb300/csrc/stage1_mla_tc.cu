@@ -45,13 +45,15 @@
 //               is ready (a separate issuer, so that neither kind of product
 //               waits behind the other's barrier);
 //   warps 4-11  the softmax. Warp w reads the S^T lanes of quarter w % 4 (16
-//               keys) for 32 of the 64 heads. The running maximum per head is
+//               keys) for 32 of the 64 heads with 16-lane tensor-memory
+//               loads, which spread the 16 x 32 scores over all 32 threads
+//               (two keys x eight heads each). The running maximum per head is
 //               lazy: it is only raised when a block's scores exceed it by
 //               more than 2^8, so most blocks need no cross-warp reduction at
 //               all, only a vote; P = exp2(s - m) then lies below 2^8, which
 //               the 16-bit P and the fp32 sums absorb. When a head's maximum
-//               is raised, the block maxima are folded over lanes (transposing
-//               xor butterfly) and quarters (shared memory), and O^T and the
+//               is raised, the block maxima are folded over threads (xor
+//               shuffles) and quarters (shared memory), and O^T and the
 //               running sums of that head are rescaled. P is rounded to one
 //               16-bit value.
 #include <type_traits>
@@ -75,29 +77,6 @@ constexpr int kSlabs = kMlaDk / 64;   // 9
 // chunk ch (0..71) of row r, 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz_off(int r, int ch, int slab_bytes) {
   return (ch >> 3) * slab_bytes + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
-}
-
-// One step of the transposing xor butterfly: lanes with `up` keep the upper
-// N values, the others the lower N, each combined with its partner's copy.
-template <int N, bool MAX>
-__device__ __forceinline__ void fold_step(float* v, int offset, bool up) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float send = up ? v[i] : v[i + N];
-    const float keep = up ? v[i + N] : v[i];
-    const float got = __shfl_xor_sync(kFull, send, offset);
-    v[i] = MAX ? fmaxf(keep, got) : keep + got;
-  }
-}
-
-// Reduce 32 columns over the 16 lanes of each half-warp (max or sum, fixed
-// order); lane l ends with columns 2 (l % 16) and 2 (l % 16) + 1 in v[0..1].
-template <bool MAX>
-__device__ __forceinline__ void fold16(float (&v)[32], int lane) {
-  fold_step<16, MAX>(v, 8, lane & 8);
-  fold_step<8, MAX>(v, 4, lane & 4);
-  fold_step<4, MAX>(v, 2, lane & 2);
-  fold_step<2, MAX>(v, 1, lane & 1);
 }
 
 // CAUSAL: several query tokens per request (q_len > 1), each row cut at its
@@ -394,33 +373,42 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     const int q = warp & 3;                         // tensor-memory lane quarter
     const int h = (warp - kMlaTcLoadWarps) >> 2;    // heads 32h .. 32h+31
     const int cl = lane & 15;
-    const int key = 16 * q + lane;                  // block key of this lane (lanes < 16)
+    // The quarter's 16 keys x the warp's 32 rows are spread over all 32
+    // threads (16-lane tensor-memory loads): value v (< 16) of this thread is
+    // key key0 + 8 ((v / 2) % 2), column 8 (v / 4) + 2 tq4 + v % 2 of the 32.
+    const int tq4 = lane & 3;
+    const int key0 = 16 * q + (lane >> 2);
+    auto col_of = [&](int v) { return 8 * (v >> 2) + 2 * tq4 + (v & 1); };
     const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
     const bool decider = q == 0;                    // warps 4 and 8 finish the reductions
     const float sl2 = a.scale_log2;
-    // running sums of P for this lane's key slot, per head, in the free
-    // tensor-memory columns 384 + 32h .. (registers are the scarce resource)
+    // running sums of P per (key slot, row), in the free tensor-memory
+    // columns 384 + 32h .. in the same 16-lane layout (registers are the
+    // scarce resource)
     const uint32_t lcols = tbase + lanes + 6 * R + 32 * h;
     // Causal cut among the query tokens: row c of this warp's 32 sees the
     // item's tokens up to vis0 + (query token of the row); blocks that end at
     // or before vis0 need no per-row test (all of them, with one token).
     const int vis0 = it.query_pos - it.tok_begin;
     const int row0 = it.grouped ? 0 : it.unit * R + 32 * h;   // first row of this warp
-    // this lane's scaled scores of block j (keys past the end or not yet
+    // this thread's 16 scaled scores of block j (keys past the end or not yet
     // visible to the row: -inf)
-    auto scores = [&](int j, int b, float (&x)[32]) {
-      uint32_t r[32];
-      tc::ld32(tbase + lanes + 4 * R + b * R + 32 * h, r);
-      const bool valid = lane < 16 && key < min(BLK, n - j * BLK);
+    auto scores = [&](int j, int b, float (&x)[16]) {
+      uint32_t r[16];
+      tc::ld16x4(tbase + lanes + 4 * R + b * R + 32 * h, r);
+      const int nv = min(BLK, n - j * BLK);
+      const bool valid0 = key0 < nv, valid1 = key0 + 8 < nv;
       if (!CAUSAL || (j + 1) * BLK - 1 <= vis0) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = valid ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+        for (int v = 0; v < 16; ++v)
+          x[v] = ((v & 2) ? valid1 : valid0) ? __uint_as_float(r[v]) * sl2 : -INFINITY;
       } else {
-        const int kj = j * BLK + key;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int tok_j = it.grouped ? 0 : (row0 + c) / a.heads;
-          x[c] = valid && kj <= vis0 + tok_j ? __uint_as_float(r[c]) * sl2 : -INFINITY;
+        for (int v = 0; v < 16; ++v) {
+          const int kj = j * BLK + key0 + 4 * (v & 2);
+          const int tok_j = it.grouped ? 0 : (row0 + col_of(v)) / a.heads;
+          x[v] = ((v & 2) ? valid1 : valid0) && kj <= vis0 + tok_j ? __uint_as_float(r[v]) * sl2
+                                                                 : -INFINITY;
         }
       }
     };
@@ -430,19 +418,19 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       const int b = j & 1;
       const bool ok = __all_sync(kFull, !*abort_flag && mbar_wait(sfull + 8 * b, (j >> 1) & 1));
       const bool o_prev = j == 0 || mbar_test(odone, (j - 1) & 1);
-      float x[32];
+      float x[16];
       bool need = j == 0;
       if (ok) {
         tc::fence_after();
         scores(j, b, x);
         if (j > 0) {
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + 32 * h + 4 * c4);
-            need |= x[4 * c4] > m4.x + kLazyRescale;
-            need |= x[4 * c4 + 1] > m4.y + kLazyRescale;
-            need |= x[4 * c4 + 2] > m4.z + kLazyRescale;
-            need |= x[4 * c4 + 3] > m4.w + kLazyRescale;
+          for (int i = 0; i < 4; ++i) {
+            const float2 m2 = *reinterpret_cast<const float2*>(m_ref + 32 * h + 8 * i + 2 * tq4);
+            need |= x[4 * i] > m2.x + kLazyRescale;
+            need |= x[4 * i + 1] > m2.y + kLazyRescale;
+            need |= x[4 * i + 2] > m2.x + kLazyRescale;
+            need |= x[4 * i + 3] > m2.y + kLazyRescale;
           }
         }
       } else {
@@ -456,10 +444,24 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           break;
         }
         // -------- slow path: raise the reference maxima of the heads that need it
-        fold16<true>(x, lane);   // block maxima over this quarter's keys
-        if (lane < 16) {
-          red[q * 64 + 32 * h + 2 * cl] = x[0];
-          red[q * 64 + 32 * h + 2 * cl + 1] = x[1];
+        {
+          // block maxima over this quarter's keys: the thread's two keys,
+          // then the eight threads that share its columns
+          float bm[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) bm[2 * i + e] = fmaxf(x[4 * i + e], x[4 * i + 2 + e]);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) bm[k] = fmaxf(bm[k], __shfl_xor_sync(kFull, bm[k], off));
+          if (lane < 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) red[q * 64 + 32 * h + 8 * i + 2 * lane + e] = bm[2 * i + e];
+          }
         }
         named_sync(1, SMX);
         if (decider && lane < 16) {
@@ -494,19 +496,31 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
           tc::fence_after();
           // scale the O^T columns of this warp's heads (all four dv tiles,
           // this quarter's lanes) and the running sums
+          // (the factors are re-read per tile: hoisted out of the loop they
+          // would hold 32 more registers across it, on this rare path)
+          const volatile float* al = alpha_s + 32 * h;
 #pragma unroll 1
-          for (int t = 0; t < 5; ++t) {
-            const uint32_t cols = t < 4 ? tbase + lanes + t * R + 32 * h : lcols;
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t cols = tbase + lanes + t * R + 32 * h;
             uint32_t o[32];
             tc::ld32(cols, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha_s[32 * h + c]);
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * al[c]);
             tc::st32(cols, o);
+          }
+          {
+            uint32_t lv[16];
+            tc::ld16x4(lcols, lv);
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              lv[v] = __float_as_uint(__uint_as_float(lv[v]) * alpha_s[32 * h + col_of(v)]);
+            tc::st16x4(lcols, lv);
           }
           tc::wait_st();
         }
-        scores(j, b, x);   // read again: the fold consumed the first copy
+        // read the scores again: keeping them live across the rescale costs
+        // more registers than this rare second load
+        scores(j, b, x);
       }
       // O of the previous block must be done before P^T is rewritten (a wait
       // that runs out stops the loop at the next vote)
@@ -515,20 +529,23 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
         *abort_flag = 1;
       // P = exp2(s - m); P^T in the inputs' 16-bit type into shared memory
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(m_ref + 32 * h + 4 * c4);
-        x[4 * c4] = ex2(x[4 * c4] - m4.x);
-        x[4 * c4 + 1] = ex2(x[4 * c4 + 1] - m4.y);
-        x[4 * c4 + 2] = ex2(x[4 * c4 + 2] - m4.z);
-        x[4 * c4 + 3] = ex2(x[4 * c4 + 3] - m4.w);
+      for (int i = 0; i < 4; ++i) {
+        const float2 m2 = *reinterpret_cast<const float2*>(m_ref + 32 * h + 8 * i + 2 * tq4);
+        x[4 * i] = ex2(x[4 * i] - m2.x);
+        x[4 * i + 1] = ex2(x[4 * i + 1] - m2.y);
+        x[4 * i + 2] = ex2(x[4 * i + 2] - m2.x);
+        x[4 * i + 3] = ex2(x[4 * i + 3] - m2.y);
       }
-      if (lane < 16) {
-        uint8_t* prow = ps + (key >> 3) * 1024 + (key & 7) * 128;
+      // two adjacent columns of one key per 4-byte store: row key, 16-byte
+      // chunk 4h + i of the 128-byte-swizzled P^T tile, word tq4
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int key = key0 + 8 * kk;
+        uint8_t* prow = ps + (key >> 3) * 1024 + (key & 7) * 128 + 4 * tq4;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(prow + (((4 * h + i) ^ (key & 7)) << 4)) = make_uint4(
-              pack2<T>(x[8 * i], x[8 * i + 1]), pack2<T>(x[8 * i + 2], x[8 * i + 3]),
-              pack2<T>(x[8 * i + 4], x[8 * i + 5]), pack2<T>(x[8 * i + 6], x[8 * i + 7]));
+          *reinterpret_cast<uint32_t*>(prow + (((4 * h + i) ^ (key & 7)) << 4)) =
+              pack2<T>(x[4 * i + 2 * kk], x[4 * i + 2 * kk + 1]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -540,12 +557,12 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
       // running sums of P in fp32 (the log-sum-exp needs them unrounded)
       {
         tc::fence_after();
-        uint32_t l[32];
-        if (j > 0) tc::ld32(lcols, l);
+        uint32_t l[16];
+        if (j > 0) tc::ld16x4(lcols, l);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          l[c] = __float_as_uint(j > 0 ? __uint_as_float(l[c]) + x[c] : x[c]);
-        tc::st32(lcols, l);
+        for (int v = 0; v < 16; ++v)
+          l[v] = __float_as_uint(j > 0 ? __uint_as_float(l[v]) + x[v] : x[v]);
+        tc::st16x4(lcols, l);
         tc::wait_st();
       }
     }
@@ -553,24 +570,34 @@ __global__ void __launch_bounds__(kMlaTcThreads, 1)
     if (!bad) {
       const bool ok = __all_sync(
           kFull, nblk == 0 || (!*abort_flag && mbar_wait(odone, (nblk - 1) & 1)));
-      float lp[32];
+      // sums over this quarter's keys: the thread's two key slots, then the
+      // eight threads that share its columns (fixed order)
+      float lp[8];
       if (nblk > 0) {
-        uint32_t l[32];
+        uint32_t l[16];
         tc::fence_after();
-        tc::ld32(lcols, l);
+        tc::ld16x4(lcols, l);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) lp[c] = __uint_as_float(l[c]);
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            lp[2 * i + e] = __uint_as_float(l[4 * i + e]) + __uint_as_float(l[4 * i + 2 + e]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+        for (int k = 0; k < 8; ++k) lp[k] = 0.f;
       }
-      fold16<false>(lp, lane);   // sums over this quarter's keys
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lp[k] += __shfl_xor_sync(kFull, lp[k], off);
       if (named_sync_or(1, SMX, !ok)) {
         bad = true;
       } else {
-        if (lane < 16) {
-          red[q * 64 + 32 * h + 2 * cl] = lp[0];
-          red[q * 64 + 32 * h + 2 * cl + 1] = lp[1];
+        if (lane < 4) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) red[q * 64 + 32 * h + 8 * i + 2 * lane + e] = lp[2 * i + e];
         }
         named_sync(1, SMX);
         if (decider && lane < 16) {
