@@ -57,23 +57,15 @@ __device__ __forceinline__ int chunk_off(int r, int cc) {
 
 // ----------------------------------------------------------- block streaming
 
-// Page id of token (block blk, row r) of the item, or 0 past the item's end:
-// a load issued blocks before the row is formed from it (kv_row_at), so that
-// its latency never stalls the warp.
-__device__ __forceinline__ int kv_page_of(const Stage1Args& a, const pkvd_work_item& it,
-                                          const int32_t* pt, int blk, int nblk, int r) {
-  const int tok = it.tok_begin + blk * BLK + r;
-  if (blk >= nblk || tok >= it.tok_end) return 0;
-  return ld_pinned(pt + tok / a.page_size);
-}
-
-// Pool row of token (block blk, row r) for the item's KV head, from its page
-// id; 0 past the item's end.
-__device__ __forceinline__ int64_t kv_row_at(const Stage1Args& a, const pkvd_work_item& it,
-                                             int blk, int nblk, int r, int page) {
+// Pool row of token (block blk, row r) of the item for its KV head, or 0 past
+// the item's end. The page-table load and the division by the page size
+// happen here, ahead of use, not when the copy is issued.
+__device__ __forceinline__ int64_t kv_row_of(const Stage1Args& a, const pkvd_work_item& it,
+                                             const int32_t* pt, int blk, int nblk, int r) {
   const int tok = it.tok_begin + blk * BLK + r;
   if (blk >= nblk || tok >= it.tok_end) return 0;
   const int pidx = tok / a.page_size;
+  int page = __ldg(pt + pidx);
   if (a.checks && (page < 0 || page >= a.num_pool_pages)) {
     atomicOr(a.status, kStatusBadPage);
     page = 0;
@@ -112,16 +104,16 @@ __device__ __forceinline__ void issue_block(const Stage1Args& a, const KvTensorM
   }
 }
 
-// Page ids of a warp's first blocks: the SPW blocks it copies first and the
-// PF blocks after them (the page-id window). Loaded at the very start of the
-// block, before the barrier set-up, so that the page-table round trip
+// Pool rows of a warp's first blocks: the SPW blocks it copies first and
+// the PF blocks after them (the page-id window). Loaded at the very start of
+// the block, before the barrier set-up, so that the page-table round trip
 // overlaps it.
 template <int D, bool TILES>
 struct WarpRows {
   static constexpr int SPW = gqa_stages_per_warp(D);
   static constexpr int PF = 4;     // page-id window (blocks)
-  int first[SPW];
-  int pages[PF];
+  int64_t first[SPW];
+  int64_t rows[PF];
   __device__ __forceinline__ WarpRows(const Stage1Args& a, const pkvd_work_item& it, int warp,
                                       int lane) {
     constexpr int W = gqa_warps(D);
@@ -130,9 +122,9 @@ struct WarpRows {
     const int r = TILES ? 0 : (lane & (BLK - 1));
     const int32_t* pt = a.page_table + static_cast<int64_t>(it.request) * a.pt_stride;
 #pragma unroll
-    for (int s = 0; s < SPW; ++s) first[s] = kv_page_of(a, it, pt, warp + W * s, nblk, r);
+    for (int s = 0; s < SPW; ++s) first[s] = kv_row_of(a, it, pt, warp + W * s, nblk, r);
 #pragma unroll
-    for (int i = 0; i < PF; ++i) pages[i] = kv_page_of(a, it, pt, warp + W * (SPW + i), nblk, r);
+    for (int i = 0; i < PF; ++i) rows[i] = kv_row_of(a, it, pt, warp + W * (SPW + i), nblk, r);
   }
 };
 
@@ -160,13 +152,12 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
   auto blk_of = [&](int k) { return warp + W * k; };
   auto stage_of = [&](int k) { return stages + (warp * SPW + k % SPW) * SB; };
   auto bar_of = [&](int k) { return bars + 8u * (warp * SPW + k % SPW); };
-  int (&pages)[PF] = wr.pages;
+  int64_t (&rows)[PF] = wr.rows;
 
 #pragma unroll
   for (int s = 0; s < SPW; ++s)
     if (s < nmine)
-      issue_block<D, TILES>(a, maps, blk_of(s), n, kv_row_at(a, it, blk_of(s), nblk, r, wr.first[s]),
-                            stage_of(s), bar_of(s), lane);
+      issue_block<D, TILES>(a, maps, blk_of(s), n, wr.first[s], stage_of(s), bar_of(s), lane);
   prologue();
 
   bool ok = true;
@@ -182,10 +173,9 @@ __device__ __forceinline__ bool gqa_warp_loop(const Stage1Args& a, const KvTenso
           process(min(BLK, n - blk * BLK), stage_of(k), blk * BLK);
           __syncwarp();
           if (k + SPW < nmine)
-            issue_block<D, TILES>(a, maps, blk_of(k + SPW), n,
-                                  kv_row_at(a, it, blk_of(k + SPW), nblk, r, pages[i]),
-                                  stage_of(k), bar_of(k), lane);
-          pages[i] = kv_page_of(a, it, pt, blk_of(k + SPW + PF), nblk, r);
+            issue_block<D, TILES>(a, maps, blk_of(k + SPW), n, rows[i], stage_of(k), bar_of(k),
+                                  lane);
+          rows[i] = kv_row_of(a, it, pt, blk_of(k + SPW + PF), nblk, r);
           ++k;
         }
       }
