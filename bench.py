@@ -114,14 +114,22 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(kernel_src: str, workload_name: str):
+def source_sha(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the kernel's source files, in order."""
+    h = hashlib.sha256()
+    for p in ([paths] if isinstance(paths, str) else paths):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_src, workload_name: str):
     """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    taken on the current kernel source (a file or a list of files); else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         with open(path) as f:
             rec = json.load(f)
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+        sha = source_sha(kernel_src)
         ent = rec.get(workload_name)
         if ent and ent.get("source_sha") == sha:
             return float(ent["bytes_per_launch"])
@@ -362,8 +370,10 @@ def prefill_arm(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-KERNEL_SRC = {"mla_tc": "stage1_mla_tc.cu", "mla_mma": "stage1_mla.cu",
-              "gqa_fma": "stage1_gqa_fma.cu", "gqa_mma": "stage1_gqa_mma.cu"}
+# a kernel's own source files (the GQA consumers share their block streaming)
+KERNEL_SRC = {"mla_tc": ("stage1_mla_tc.cu",), "mla_mma": ("stage1_mla.cu",),
+              "gqa_fma": ("stage1_gqa_fma.cu", "stage1_gqa.cuh"),
+              "gqa_mma": ("stage1_gqa_mma.cu", "stage1_gqa.cuh")}
 
 
 class Timer:
@@ -472,7 +482,8 @@ def measure(name, args, timer, clock_index, steps, warmup):
     kv = case.kv_bytes_unique()
     kern = stage1_kernel_name(plan)
     traffic = recorded_traffic(
-        os.path.join(ROOT, "paged_kv_cache_plan_gb300", "csrc", KERNEL_SRC[kern]), case.name)
+        [os.path.join(ROOT, "paged_kv_cache_plan_gb300", "csrc", f) for f in KERNEL_SRC[kern]],
+        case.name)
     info = plan.info
     rec = {
         "workload": case.name, "us_per_op": round(ms * 1e3, 2),
