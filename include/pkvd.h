@@ -200,7 +200,9 @@ int decode_plan(pkvd_plan **out, int batch, int heads, int kv_heads, int head_di
  * planner, allocates and fills the device work list and the partial
  * workspace. *out receives the plan (NULL on error). PKVD_EINVAL for a bad
  * field, PKVD_EUNSUPPORTED for a shape no kernel takes, PKVD_ENOMEM /
- * PKVD_ECUDA if the device allocation or upload failed.
+ * PKVD_ECUDA if the device allocation or upload failed. The fields and
+ * seq_lens are checked before the kernel variant, so a request shorter than
+ * q_len gives PKVD_EINVAL even for a shape no variant takes.
  * Defined by: aiter pull 4758, Motivation (split count) and Technical
  * Details 2 (split-major grid order) and 3 (head-dim-tiled merge gated on
  * idle SMs); ROCm/rocm-libraries pull 10102, Motivation (a launch must be

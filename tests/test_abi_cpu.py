@@ -438,3 +438,70 @@ def test_query_token_plans_cover_every_token_once(L):
                          ((2, 16, 1, 576, 1), [2000, 70], 4)):
         info, items = _plan(*args, seq=seq, q_len=q)
         _check_cover(info, items, seq, info["units_per_request"])
+
+
+def _random_case(rng):
+    # one seeded planner case inside the documented domain: GQA (head_dim 128
+    # or 256, q_len * group <= 16) or MLA shape, a length mix with empty and
+    # one-token requests (every non-empty request holds its q_len queries),
+    # auto or forced splits, any grid order
+    batch = rng.randint(1, 12)
+    if rng.random() < 0.5:
+        kv = rng.choice((1, 2, 4, 8))
+        group = rng.choice((1, 2, 4, 8, 16))
+        args = (batch, kv * group, kv, rng.choice((128, 256)), rng.choice((1, 16, 64)))
+        q_len = rng.randint(1, min(4, 16 // group))
+    else:
+        args = (batch, rng.choice((16, 32, 48, 64, 128)), 1, 576, rng.choice((1, 64)))
+        q_len = rng.randint(1, 4)
+    seq = [rng.choice((0, q_len, rng.randint(2, 300), rng.randint(300, 20000),
+                       rng.randint(20000, 140000))) for _ in range(batch)]
+    seq = [L and max(L, q_len) for L in seq]
+    kw = dict(q_len=q_len, grid_order=rng.choice(("auto", "split_major", "request_major")),
+              ctas_per_sm=rng.choice((1, 2)))
+    if rng.random() < 0.4:
+        kw["splits"] = rng.randint(1, 300)
+    return args, seq, kw
+
+
+def test_random_plans_cover_every_token_once(L):
+    import random
+    rng = random.Random(20261202)
+    checked = 0
+    for _ in range(300):
+        args, seq, kw = _random_case(rng)
+        if not any(seq):
+            continue
+        info, items = _plan(*args, seq=seq, **kw)
+        assert info["num_items"] == len(items)
+        _check_cover(info, items, seq, info["units_per_request"])
+        # the split count of a request never exceeds what was asked or its tokens
+        per = {}
+        for (b, u, s, *_rest) in items:
+            per[(b, u)] = max(per.get((b, u), 0), s + 1)
+        assert max(per.values()) == info["max_splits"]
+        for (b, u), n in per.items():
+            assert n <= seq[b]
+            if "splits" in kw:
+                assert n <= kw["splits"]
+        checked += 1
+    assert checked > 250
+
+
+def test_random_refusals_follow_the_documented_domain(L):
+    import random
+    rng = random.Random(7)
+    for _ in range(100):
+        args, seq, kw = _random_case(rng)
+        q = kw["q_len"] = rng.randint(2, 8)
+        # argument checks (lengths) come before the shape checks
+        if any(0 < L < q for L in seq):
+            code = _lib.PKVD_EINVAL             # a request shorter than its queries
+        elif args[3] != 576 and q * (args[1] // args[2]) > 16:
+            code = _lib.PKVD_EUNSUPPORTED       # more query rows than one 16-row tile
+        else:
+            _plan(*args, seq=seq, **kw)
+            continue
+        with pytest.raises(_lib.PkvdError) as e:
+            _plan(*args, seq=seq, **kw)
+        assert e.value.code == code, (args, seq, kw)
