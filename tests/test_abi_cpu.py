@@ -268,6 +268,35 @@ def test_shared_prefix_plan_covers_every_token_once(L):
         assert t1 - t0 >= 1024 or t1 == plen[b0]
 
 
+def test_random_shared_prefix_plans_cover_every_token_once(L):
+    # seeded mixes of groups (runs of 1 to 8 consecutive requests), ungrouped
+    # requests and empty ones, short and long prefixes
+    import random
+    rng = random.Random(31)
+    for _ in range(150):
+        heads = rng.choice((16, 32, 64))
+        seq, groups, plen = [], [], []
+        g = 0
+        while len(seq) < rng.randint(1, 14):
+            if rng.random() < 0.3:
+                seq.append(rng.choice((0, 1, rng.randint(2, 30000))))
+                groups.append(-1)
+                plen.append(0)
+                continue
+            n, p = rng.randint(1, 8), rng.choice((1, rng.randint(2, 1023),
+                                                  rng.randint(1024, 60000)))
+            for _ in range(n):
+                seq.append(p + rng.choice((0, 1, rng.randint(2, 5000))))
+                groups.append(g)
+                plen.append(p)
+            g += 1
+        info, pre, rest = _prefix_plan(len(seq), heads, seq, groups, plen,
+                                       ctas_per_sm=rng.choice((1, 2)))
+        _check_prefix_cover(seq, groups, plen, info, pre, rest)
+        for (b0, unit, *_rest) in pre:
+            assert unit <= 64 // heads and plen[b0] >= 1024
+
+
 @pytest.mark.parametrize("prefix", [1, 64, 500, 1023])
 def test_short_shared_prefix_is_not_grouped(L, prefix):
     # the grouped items run on the tensor-memory kernel, whose one-part P is
